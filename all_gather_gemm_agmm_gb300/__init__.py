@@ -1,0 +1,245 @@
+"""GB300 (sm_103a) fused all-gather matmul: a thin Python binding of libagmm.so.
+
+    O = concat(X_0, ..., X_{P-1}) @ (Y if not rhs_transpose else Y.T)
+
+Every step of the computation runs in the CUDA kernels of ``libagmm.so``
+(``include/agmm.h``); this module only marshals arguments through ctypes.
+PyTorch supplies device memory and streams.  There is no CPU fallback: if the
+library is missing or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libagmm.so")
+
+# Status codes of agmm.h.
+AGMM_OK = 0
+AGMM_ERR_INVALID_ARG = 1
+AGMM_ERR_UNSUPPORTED = 2
+AGMM_ERR_ALIGNMENT = 3
+AGMM_ERR_CUDA = 4
+AGMM_ERR_TIMEOUT = 5
+AGMM_ERR_NOMEM = 6
+AGMM_BF16 = 0
+AGMM_BF16_F32OUT = 1
+
+# Every symbol agmm.h declares.
+EXPORTED_SYMBOLS = [
+    "agmm_plan", "agmm_destroy", "agmm_workspace_bytes", "agmm_run", "agmm_run_unfused",
+    "agmm_run_host", "agmm_query_status", "agmm_plan_info", "agmm_ring_chunks",
+    "agmm_status_string", "agmm_last_error", "agmm_version",
+]
+
+
+class AgmmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("path", ctypes.c_int), ("box_rows", ctypes.c_int), ("chunks", ctypes.c_int),
+        ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int),
+        ("stages", ctypes.c_int), ("splits", ctypes.c_int), ("num_tiles", ctypes.c_int),
+        ("num_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("num_sms", ctypes.c_int),
+        ("smem_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libagmm.so (built by ``__graft_entry__.build()``) and declare its ABI."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, i64, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.agmm_plan.argtypes = [c_int, i64, i64, i64, c_int, c_int, ctypes.POINTER(vp)]
+    lib.agmm_plan.restype = c_int
+    lib.agmm_destroy.argtypes = [vp]
+    lib.agmm_destroy.restype = None
+    lib.agmm_workspace_bytes.argtypes = [vp, c_int]
+    lib.agmm_workspace_bytes.restype = ctypes.c_size_t
+    lib.agmm_run.argtypes = [vp, ctypes.POINTER(vp), vp, vp, c_int, vp, vp]
+    lib.agmm_run.restype = c_int
+    lib.agmm_run_unfused.argtypes = [vp, ctypes.POINTER(vp), vp, vp, c_int, vp, vp]
+    lib.agmm_run_unfused.restype = c_int
+    lib.agmm_run_host.argtypes = [vp, ctypes.POINTER(vp), vp, vp, ctypes.POINTER(vp), vp, vp, c_int, vp, vp]
+    lib.agmm_run_host.restype = c_int
+    lib.agmm_query_status.argtypes = [vp, vp, vp]
+    lib.agmm_query_status.restype = c_int
+    lib.agmm_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+    lib.agmm_plan_info.restype = c_int
+    lib.agmm_ring_chunks.argtypes = [c_int, i64, c_int, c_int, ctypes.POINTER(ctypes.c_int32),
+                                     ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_int32),
+                                     i64, ctypes.POINTER(i64)]
+    lib.agmm_ring_chunks.restype = c_int
+    lib.agmm_status_string.argtypes = [c_int]
+    lib.agmm_status_string.restype = ctypes.c_char_p
+    lib.agmm_last_error.argtypes = []
+    lib.agmm_last_error.restype = ctypes.c_char_p
+    lib.agmm_version.argtypes = []
+    lib.agmm_version.restype = c_int
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def _status_name(status: int) -> str:
+    names = {0: "AGMM_OK", 1: "AGMM_ERR_INVALID_ARG", 2: "AGMM_ERR_UNSUPPORTED", 3: "AGMM_ERR_ALIGNMENT",
+             4: "AGMM_ERR_CUDA", 5: "AGMM_ERR_TIMEOUT", 6: "AGMM_ERR_NOMEM"}
+    return names.get(status, f"AGMM_STATUS_{status}")
+
+
+def _check(status: int) -> None:
+    if status != AGMM_OK:
+        raise AgmmError(status, load_library().agmm_last_error().decode())
+
+
+def _ptr_array(ptrs: Sequence[int]):
+    return (ctypes.c_void_p * len(ptrs))(*[ctypes.c_void_p(int(p)) for p in ptrs])
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def ring_chunks(P: int, m_per_device: int, my_id: int, box_rows: int) -> Dict[str, List[int]]:
+    """The ring-ordered row chunks (host logic of agmm_ring_chunks)."""
+    lib = load_library()
+    n = ctypes.c_int64(0)
+    _check(lib.agmm_ring_chunks(P, m_per_device, my_id, box_rows, None, None, None, None, 0, ctypes.byref(n)))
+    cnt = n.value
+    shard = (ctypes.c_int32 * cnt)()
+    src = (ctypes.c_int64 * cnt)()
+    out = (ctypes.c_int64 * cnt)()
+    valid = (ctypes.c_int32 * cnt)()
+    _check(lib.agmm_ring_chunks(P, m_per_device, my_id, box_rows, shard, src, out, valid, cnt, ctypes.byref(n)))
+    return {"shard": list(shard), "src_row": list(src), "out_row": list(out), "valid": list(valid)}
+
+
+class Plan:
+    """A planned problem: P shards of [m_per_device, k] times Y ([k, n] or [n, k])."""
+
+    def __init__(self, P: int, m_per_device: int, k: int, n: int, rhs_transpose: bool = False,
+                 out_f32: bool = False):
+        self._lib = load_library()
+        self.P, self.m_per_device, self.k, self.n = int(P), int(m_per_device), int(k), int(n)
+        self.rhs_transpose = bool(rhs_transpose)
+        self.out_f32 = bool(out_f32)
+        h = ctypes.c_void_p()
+        _check(self._lib.agmm_plan(self.P, self.m_per_device, self.k, self.n,
+                                   AGMM_BF16_F32OUT if out_f32 else AGMM_BF16, int(self.rhs_transpose),
+                                   ctypes.byref(h)))
+        self._h = h
+
+    @property
+    def M(self) -> int:
+        return self.P * self.m_per_device
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self._lib.agmm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def info(self) -> Dict[str, int]:
+        inf = PlanInfo()
+        _check(self._lib.agmm_plan_info(self._h, ctypes.byref(inf)))
+        return {f: getattr(inf, f) for f, _ in PlanInfo._fields_}
+
+    def workspace_bytes(self, unfused: bool = False) -> int:
+        return int(self._lib.agmm_workspace_bytes(self._h, int(bool(unfused))))
+
+    def new_workspace(self, unfused: bool = False, device=None):
+        import torch
+
+        return torch.zeros(self.workspace_bytes(unfused), dtype=torch.uint8, device=device or "cuda")
+
+    def run(self, xs, y, o, my_id: int, workspace, stream=None) -> None:
+        """Fused path.  xs: P device tensors; y, o, workspace: device tensors."""
+        _check(self._lib.agmm_run(self._h, _ptr_array([x.data_ptr() for x in xs]), y.data_ptr(), o.data_ptr(),
+                                  int(my_id), workspace.data_ptr(), _stream_handle(stream)))
+
+    def run_ptrs(self, x_ptrs: Sequence[int], y_ptr: int, o_ptr: int, my_id: int, ws_ptr: int,
+                 stream_handle: Optional[int]) -> None:
+        _check(self._lib.agmm_run(self._h, _ptr_array(x_ptrs), y_ptr, o_ptr, int(my_id), ws_ptr, stream_handle))
+
+    def run_unfused(self, xs, y, o, my_id: int, workspace, stream=None) -> None:
+        """Gather into the workspace, then the same GEMM on the gathered buffer."""
+        _check(self._lib.agmm_run_unfused(self._h, _ptr_array([x.data_ptr() for x in xs]), y.data_ptr(),
+                                          o.data_ptr(), int(my_id), workspace.data_ptr(), _stream_handle(stream)))
+
+    def run_host(self, xs_host, y_host, o_host, xs_dev, y_dev, o_dev, my_id: int, workspace, stream=None) -> None:
+        """Upload host inputs, run the fused path, download O (asynchronous)."""
+        _check(self._lib.agmm_run_host(self._h, _ptr_array([x.data_ptr() for x in xs_host]), y_host.data_ptr(),
+                                       o_host.data_ptr(), _ptr_array([x.data_ptr() for x in xs_dev]),
+                                       y_dev.data_ptr(), o_dev.data_ptr(), int(my_id), workspace.data_ptr(),
+                                       _stream_handle(stream)))
+
+    def query_status(self, workspace, stream=None) -> int:
+        """Synchronize and return (and clear) the device status; raises on error."""
+        st = self._lib.agmm_query_status(self._h, workspace.data_ptr(), _stream_handle(stream))
+        _check(st)
+        return st
+
+
+def _check_operands(xs, y, rhs_transpose: bool):
+    import torch
+
+    if len(xs) < 1:
+        raise ValueError("need at least one shard")
+    m, k = xs[0].shape
+    for x in xs:
+        if x.dtype != torch.bfloat16 or y.dtype != torch.bfloat16:
+            raise ValueError("inputs must be bfloat16")
+        if x.shape != (m, k) or not x.is_contiguous() or not x.is_cuda:
+            raise ValueError("shards must be contiguous CUDA tensors of one shape")
+    if y.dim() != 2 or not y.is_contiguous() or not y.is_cuda:
+        raise ValueError("y must be a contiguous 2-D CUDA tensor")
+    n, ky = (y.shape if rhs_transpose else (y.shape[1], y.shape[0]))
+    if ky != k:
+        raise ValueError(f"contracting dimension mismatch: shards have k={k}, y gives {ky}")
+    return m, k, n
+
+
+_plan_cache: Dict[tuple, Plan] = {}
+
+
+def all_gather_matmul(xs, y, my_id: int = 0, rhs_transpose: bool = False, out=None, unfused: bool = False,
+                      out_f32: bool = False, workspace=None, stream=None):
+    """all-gather(xs, axis=0) @ y on one GPU; returns O [P*m, n] (bf16 or float32)."""
+    import torch
+
+    m, k, n = _check_operands(xs, y, rhs_transpose)
+    key = (len(xs), m, k, n, bool(rhs_transpose), bool(out_f32), torch.cuda.current_device())
+    plan = _plan_cache.get(key)
+    if plan is None:
+        plan = Plan(len(xs), m, k, n, rhs_transpose, out_f32)
+        _plan_cache[key] = plan
+    if out is None:
+        out = torch.empty((plan.M, n), dtype=torch.float32 if out_f32 else torch.bfloat16, device=y.device)
+    if workspace is None:
+        workspace = plan.new_workspace(unfused, device=y.device)
+    (plan.run_unfused if unfused else plan.run)(xs, y, out, my_id, workspace, stream)
+    return out

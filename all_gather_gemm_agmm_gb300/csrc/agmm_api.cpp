@@ -1,0 +1,515 @@
+// agmm_api.cpp -- the C ABI of include/agmm.h: argument validation, tile
+// planning, the per-shard TMA descriptor table, and kernel launches.
+//
+// Validation follows validate_inputs of tpu_inference "all_gather_matmul.py"
+// (k % 128, n % 128), with its m rules relaxed (see agmm.h).  The descriptor
+// table follows the per-peer descriptor idea of jax mosaic gpu
+// "launch_context.py" (_get_tma_desc: one 128-byte descriptor per peer base
+// pointer, at most 8 peers): descriptors are encoded on the host and passed to
+// the kernel as a __grid_constant__ parameter block.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "agmm.h"
+#include "kernel_params.h"
+#include "ring_schedule.h"
+
+using namespace agmm;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+agmm_status_t fail(agmm_status_t s, const std::string& msg) {
+  g_last_error = msg;
+  if (std::getenv("AGMM_LOG")) std::fprintf(stderr, "[agmm] %s: %s\n", agmm_status_string(s), msg.c_str());
+  return s;
+}
+
+agmm_status_t fail_cuda(cudaError_t e, const char* what) {
+  return fail(AGMM_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::atoi(v);
+}
+
+constexpr int64_t kMaxElems = (int64_t)1 << 40;
+constexpr size_t kMaxDynSmem = 232448;  // 227 KiB per CTA on sm_100-class parts
+
+int pow2_ceil(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+               uint32_t box_outer, std::string* err) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+struct agmm_plan_s {
+  int P = 0;
+  int64_t m_pd = 0, k = 0, n = 0;
+  agmm_dtype_t dtype = AGMM_BF16;
+  int rhs_t = 0;
+  int device = 0;
+  int num_sms = 0;
+  KernelKey key{};
+  int box_rows = 0, total_chunks = 0, num_m_tiles = 0, num_n_tiles = 0, num_k_blocks = 0;
+  int group_m = 1, num_tiles = 0, stages = 0, mma_n = 0, tmem_cols = 0, splits = 1;
+  uint32_t b_slot_bytes = 0;
+  size_t smem_bytes = 0;
+  dim3 grid{1, 1, 1};
+  int cluster_x = 1;
+  // descriptor cache: tensor maps depend only on the X and Y pointers
+  bool cache_valid = false;
+  const void* cache_x[kMaxShards] = {};
+  const void* cache_y = nullptr;
+  KernelParams params{};
+  agmm_plan_s* sub = nullptr;  // unfused path: P = 1 over the gathered buffer
+  size_t out_elem = 2;
+  int64_t M() const { return (int64_t)P * m_pd; }
+};
+
+namespace {
+
+agmm_status_t validate_shape(int P, int64_t m_pd, int64_t k, int64_t n, int dtype, int rhs_t) {
+  if (P < 1 || P > AGMM_MAX_SHARDS)
+    return fail(AGMM_ERR_INVALID_ARG, "P must be in [1, 8] (per-peer descriptor tables hold at most 8)");
+  if (m_pd < 1 || m_pd > ((int64_t)1 << 31) - 1)
+    return fail(AGMM_ERR_INVALID_ARG, "m_per_device must be in [1, 2^31)");
+  if (k < 128 || k % 128 != 0) return fail(AGMM_ERR_INVALID_ARG, "k must be a positive multiple of 128");
+  if (n < 128 || n % 128 != 0) return fail(AGMM_ERR_INVALID_ARG, "n must be a positive multiple of 128");
+  if (k > ((int64_t)1 << 31) - 1 || n > ((int64_t)1 << 31) - 1)
+    return fail(AGMM_ERR_INVALID_ARG, "k and n must be below 2^31");
+  const int64_t M = (int64_t)P * m_pd;
+  if (M > kMaxElems / k || k > kMaxElems / n || M > kMaxElems / n)
+    return fail(AGMM_ERR_INVALID_ARG, "problem exceeds 2^40 elements in an operand");
+  if (dtype != AGMM_BF16 && dtype != AGMM_BF16_F32OUT) return fail(AGMM_ERR_INVALID_ARG, "unknown dtype");
+  if (rhs_t != 0 && rhs_t != 1) return fail(AGMM_ERR_INVALID_ARG, "rhs_transpose must be 0 or 1");
+  return AGMM_OK;
+}
+
+// Tile planning for a device with `num_sms` SMs (pure host logic).
+agmm_status_t choose_tiles(agmm_plan_s* pl) {
+  const int force_path = env_int("AGMM_PATH", -1);
+  // Swap path: the whole ring-ordered row sequence (chunks padded to their box
+  // height) fits in one MMA N of at most 256.  Pick the box height with the
+  // least padding, the largest on ties (fewer TMA boxes).
+  int best_bh = -1;
+  int64_t best_pad = 0;
+  for (int bh = 128; bh >= 8; bh >>= 1) {
+    const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh);
+    const int64_t pad = ring_padded_rows(g);
+    if (pad <= 256 && (best_bh < 0 || pad < best_pad)) {
+      best_bh = bh;
+      best_pad = pad;
+    }
+  }
+  const int64_t budget = (int64_t)kMaxDynSmem - 1024 - 256;
+  pl->num_k_blocks = (int)(pl->k / kTileK);
+  if (best_bh > 0 && force_path != kPathRows) {
+    pl->key.path = kPathSwap;
+    pl->key.bn = kTileM;
+    pl->box_rows = best_bh;
+    pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, best_bh));
+    pl->mma_n = (int)((best_pad + 31) / 32 * 32);
+    pl->num_n_tiles = (int)(pl->n / kTileM);
+    pl->num_m_tiles = 1;
+    pl->num_tiles = pl->num_n_tiles;
+    pl->b_slot_bytes = (uint32_t)pl->mma_n * 128u;
+    const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
+    pl->stages = (int)std::min<int64_t>(kMaxStages, budget / stage_bytes);
+    pl->stages = std::min(pl->stages, std::max(2, env_int("AGMM_STAGES", kMaxStages)));
+    while ((int64_t)pl->stages * stage_bytes < (int64_t)pl->mma_n * kTileM * 4) ++pl->stages;
+    int splits = pl->num_sms / pl->num_n_tiles;
+    splits = std::max(1, std::min(splits, std::min(8, pl->num_k_blocks)));
+    const int env_splits = env_int("AGMM_SPLITK", 0);
+    if (env_splits > 0) splits = std::max(1, std::min(env_splits, std::min(16, pl->num_k_blocks)));
+    pl->splits = splits;
+    pl->tmem_cols = pow2_ceil(std::max(32, pl->mma_n));
+    pl->group_m = 1;
+  } else {
+    pl->key.path = kPathRows;
+    // Box height: fewest 128-row tiles, the largest box on ties.
+    int bh_best = 128;
+    int64_t tiles_best = -1;
+    for (int bh = 128; bh >= 8; bh >>= 1) {
+      const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh);
+      const int64_t cpt = kTileM / bh;
+      const int64_t t = (ring_total_chunks(g) + cpt - 1) / cpt;
+      if (tiles_best < 0 || t < tiles_best) {
+        tiles_best = t;
+        bh_best = bh;
+      }
+    }
+    if (tiles_best > (int64_t)1 << 30) return fail(AGMM_ERR_INVALID_ARG, "too many row tiles");
+    int bn = (pl->n % 256 == 0) ? 256 : 128;
+    const int env_bn = env_int("AGMM_BN", 0);
+    if ((env_bn == 128 || env_bn == 256) && pl->n % env_bn == 0) bn = env_bn;
+    pl->key.bn = bn;
+    pl->box_rows = bh_best;
+    pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, bh_best));
+    pl->num_m_tiles = (int)tiles_best;
+    pl->num_n_tiles = (int)(pl->n / bn);
+    if ((int64_t)pl->num_m_tiles * pl->num_n_tiles > ((int64_t)1 << 31) - 1)
+      return fail(AGMM_ERR_INVALID_ARG, "too many output tiles");
+    pl->num_tiles = pl->num_m_tiles * pl->num_n_tiles;
+    pl->mma_n = bn;
+    pl->b_slot_bytes = (uint32_t)bn * 128u;
+    const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
+    pl->stages = (int)std::min<int64_t>(kMaxStages, budget / stage_bytes);
+    pl->stages = std::min(pl->stages, std::max(2, env_int("AGMM_STAGES", kMaxStages)));
+    pl->splits = 1;
+    pl->tmem_cols = 2 * bn;
+    pl->group_m = std::max(1, env_int("AGMM_GROUP_M", 8));
+  }
+  pl->smem_bytes = 1024 + (size_t)pl->stages * (kASlotBytes + pl->b_slot_bytes) + 256;
+  return AGMM_OK;
+}
+
+agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t dtype, int rhs_t,
+                        bool with_sub, agmm_plan_s** out) {
+  agmm_status_t st = validate_shape(P, m_pd, k, n, (int)dtype, rhs_t);
+  if (st != AGMM_OK) return st;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  int major = 0, minor = 0, sms = 0;
+  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return fail_cuda(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(AGMM_ERR_UNSUPPORTED, "this library is built for sm_103a only; device is sm_" +
+                                          std::to_string(major) + std::to_string(minor));
+  agmm_plan_s* pl = new (std::nothrow) agmm_plan_s();
+  if (!pl) return fail(AGMM_ERR_NOMEM, "plan allocation");
+  pl->P = P;
+  pl->m_pd = m_pd;
+  pl->k = k;
+  pl->n = n;
+  pl->dtype = dtype;
+  pl->rhs_t = rhs_t;
+  pl->device = dev;
+  pl->num_sms = sms;
+  pl->key.y_kmajor = rhs_t != 0;
+  pl->key.out_f32 = dtype == AGMM_BF16_F32OUT;
+  pl->out_elem = pl->key.out_f32 ? 4 : 2;
+  st = choose_tiles(pl);
+  if (st != AGMM_OK) {
+    delete pl;
+    return st;
+  }
+  // Attributes and co-residency: shrink the cluster until it can be scheduled.
+  for (;;) {
+    int active = 0;
+    e = prepare_agmm_kernel(pl->key, pl->smem_bytes, pl->splits, &active);
+    if (e != cudaSuccess) {
+      delete pl;
+      return fail_cuda(e, "kernel attribute setup");
+    }
+    if (active > 0) break;
+    if (pl->splits <= 1) {
+      delete pl;
+      return fail(AGMM_ERR_UNSUPPORTED, "kernel cannot be resident with the planned shared memory");
+    }
+    pl->splits = std::max(1, pl->splits / 2);
+  }
+  if (pl->key.path == kPathSwap) {
+    pl->grid = dim3((unsigned)pl->splits, (unsigned)pl->num_n_tiles, 1);
+    pl->cluster_x = pl->splits;
+  } else {
+    pl->grid = dim3((unsigned)std::min(pl->num_tiles, pl->num_sms), 1, 1);
+    pl->cluster_x = 1;
+  }
+  KernelParams& kp = pl->params;
+  kp.m_pd = m_pd;
+  kp.ldo = n;
+  kp.P = P;
+  kp.box_rows = pl->box_rows;
+  kp.total_chunks = pl->total_chunks;
+  kp.num_m_tiles = pl->num_m_tiles;
+  kp.num_n_tiles = pl->num_n_tiles;
+  kp.num_k_blocks = pl->num_k_blocks;
+  kp.group_m = pl->group_m;
+  kp.num_tiles = pl->num_tiles;
+  kp.stages = pl->stages;
+  kp.mma_n = pl->mma_n;
+  kp.tmem_cols = pl->tmem_cols;
+  kp.splits = pl->splits;
+  kp.b_slot_bytes = pl->b_slot_bytes;
+  kp.wait_limit_ns = (uint64_t)std::max(1, env_int("AGMM_WAIT_LIMIT_MS", 2000)) * 1000000ull;
+  kp.test_drop_first_arrive = env_int("AGMM_TEST_DROP_ARRIVE", 0) != 0;
+  if (with_sub && P > 1) {
+    st = plan_impl(1, pl->M(), k, n, dtype, rhs_t, false, &pl->sub);
+    if (st != AGMM_OK) {
+      delete pl;
+      return st;
+    }
+  }
+  *out = pl;
+  return AGMM_OK;
+}
+
+agmm_status_t check_run_args(agmm_plan_s* pl, const void* const* xs, const void* y, void* o, int my_id,
+                             void* ws) {
+  if (!pl) return fail(AGMM_ERR_INVALID_ARG, "plan is NULL");
+  if (!xs || !y || !o || !ws) return fail(AGMM_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (my_id < 0 || my_id >= pl->P) return fail(AGMM_ERR_INVALID_ARG, "my_id must be in [0, P)");
+  const size_t xbytes = (size_t)pl->m_pd * (size_t)pl->k * 2;
+  const size_t ybytes = (size_t)pl->k * (size_t)pl->n * 2;
+  const size_t obytes = (size_t)pl->M() * (size_t)pl->n * pl->out_elem;
+  for (int r = 0; r < pl->P; ++r) {
+    if (!xs[r]) return fail(AGMM_ERR_INVALID_ARG, "shard pointer " + std::to_string(r) + " is NULL");
+    if (!aligned16(xs[r])) return fail(AGMM_ERR_ALIGNMENT, "shard " + std::to_string(r) + " is not 16-byte aligned");
+    if (overlaps(xs[r], xbytes, o, obytes)) return fail(AGMM_ERR_INVALID_ARG, "O overlaps a shard");
+  }
+  if (!aligned16(y) || !aligned16(o) || !aligned16(ws))
+    return fail(AGMM_ERR_ALIGNMENT, "Y, O and the workspace must be 16-byte aligned");
+  if (overlaps(y, ybytes, o, obytes)) return fail(AGMM_ERR_INVALID_ARG, "O overlaps Y");
+  return AGMM_OK;
+}
+
+agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y, void* o, int my_id,
+                           void* ws, cudaStream_t stream) {
+  bool same = pl->cache_valid && pl->cache_y == y;
+  for (int r = 0; same && r < pl->P; ++r) same = pl->cache_x[r] == xs[r];
+  KernelParams& kp = pl->params;
+  if (!same) {
+    std::string err;
+    for (int r = 0; r < pl->P; ++r) {
+      if (!encode_2d(&kp.xmap[r], xs[r], (uint64_t)pl->k, (uint64_t)pl->m_pd, kTileK, (uint32_t)pl->box_rows, &err)) {
+        pl->cache_valid = false;
+        return fail(AGMM_ERR_CUDA, "shard tensor map: " + err);
+      }
+    }
+    bool ok;
+    const uint32_t y_rows = pl->key.path == kPathSwap ? (uint32_t)kTileM : (uint32_t)pl->key.bn;
+    if (pl->rhs_t)  // Y [n, k]: K-major boxes of y_rows n-rows
+      ok = encode_2d(&kp.ymap, y, (uint64_t)pl->k, (uint64_t)pl->n, kTileK, y_rows, &err);
+    else  // Y [k, n]: MN-major boxes of 64 n x 64 k
+      ok = encode_2d(&kp.ymap, y, (uint64_t)pl->n, (uint64_t)pl->k, 64, kTileK, &err);
+    if (!ok) {
+      pl->cache_valid = false;
+      return fail(AGMM_ERR_CUDA, "Y tensor map: " + err);
+    }
+    for (int r = 0; r < pl->P; ++r) pl->cache_x[r] = xs[r];
+    pl->cache_y = y;
+    pl->cache_valid = true;
+  }
+  kp.out = o;
+  kp.status = static_cast<int*>(ws);
+  kp.my_id = my_id;
+  cudaError_t e = launch_agmm_kernel(pl->key, kp, pl->grid, pl->cluster_x, pl->smem_bytes, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "fused kernel launch");
+  return AGMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+agmm_status_t agmm_plan(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
+                        int rhs_transpose, agmm_plan_t* out_plan) {
+  if (!out_plan) return fail(AGMM_ERR_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  agmm_plan_s* pl = nullptr;
+  agmm_status_t st = plan_impl(P, m_per_device, k, n, dtype, rhs_transpose, true, &pl);
+  if (st == AGMM_OK) *out_plan = pl;
+  return st;
+}
+
+void agmm_destroy(agmm_plan_t plan) {
+  if (!plan) return;
+  agmm_destroy(plan->sub);
+  delete plan;
+}
+
+size_t agmm_workspace_bytes(agmm_plan_t plan, int unfused) {
+  if (!plan) return 0;
+  size_t b = kStatusBytes;
+  if (unfused) b += ((size_t)plan->M() * (size_t)plan->k * 2 + 255) / 256 * 256;
+  return b;
+}
+
+agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o, int my_id,
+                       void* workspace, void* stream) {
+  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace);
+  if (st != AGMM_OK) return st;
+  return launch_fused(plan, x_shards, y, o, my_id, workspace, static_cast<cudaStream_t>(stream));
+}
+
+agmm_status_t agmm_run_unfused(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o,
+                               int my_id, void* workspace, void* stream) {
+  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace);
+  if (st != AGMM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (plan->P == 1) return launch_fused(plan, x_shards, y, o, 0, workspace, s);
+  uint8_t* gathered = static_cast<uint8_t*>(workspace) + kStatusBytes;
+  const size_t gbytes = (size_t)plan->M() * (size_t)plan->k * 2;
+  for (int r = 0; r < plan->P; ++r)
+    if (overlaps(x_shards[r], (size_t)plan->m_pd * plan->k * 2, gathered, gbytes))
+      return fail(AGMM_ERR_INVALID_ARG, "the workspace overlaps a shard");
+  GatherParams g{};
+  for (int r = 0; r < plan->P; ++r) g.src[r] = static_cast<const uint4*>(x_shards[r]);
+  g.dst = reinterpret_cast<uint4*>(gathered);
+  g.vec_per_shard = plan->m_pd * plan->k * 2 / 16;
+  const int64_t want = (g.vec_per_shard + 4 * 256 - 1) / (4 * 256);
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)plan->num_sms * 8 / plan->P + 1));
+  cudaError_t e = launch_gather_kernel(g, plan->P, blocks, s);
+  if (e != cudaSuccess) return fail_cuda(e, "gather kernel launch");
+  const void* one[1] = {gathered};
+  return launch_fused(plan->sub, one, y, o, 0, workspace, s);
+}
+
+agmm_status_t agmm_run_host(agmm_plan_t plan, const void* const* x_host, const void* y_host, void* o_host,
+                            void* const* x_dev, void* y_dev, void* o_dev, int my_id, void* workspace,
+                            void* stream) {
+  if (!plan || !x_host || !y_host || !o_host || !x_dev)
+    return fail(AGMM_ERR_INVALID_ARG, "a pointer argument is NULL");
+  for (int r = 0; r < plan->P; ++r)
+    if (!x_host[r] || !x_dev[r]) return fail(AGMM_ERR_INVALID_ARG, "a shard pointer is NULL");
+  agmm_status_t st = check_run_args(plan, const_cast<const void* const*>(x_dev), y_dev, o_dev, my_id, workspace);
+  if (st != AGMM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t xbytes = (size_t)plan->m_pd * plan->k * 2;
+  cudaError_t e;
+  for (int r = 0; r < plan->P; ++r)
+    if ((e = cudaMemcpyAsync(x_dev[r], x_host[r], xbytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return fail_cuda(e, "shard upload");
+  if ((e = cudaMemcpyAsync(y_dev, y_host, (size_t)plan->k * plan->n * 2, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return fail_cuda(e, "Y upload");
+  st = launch_fused(plan, const_cast<const void* const*>(x_dev), y_dev, o_dev, my_id, workspace, s);
+  if (st != AGMM_OK) return st;
+  if ((e = cudaMemcpyAsync(o_host, o_dev, (size_t)plan->M() * plan->n * plan->out_elem, cudaMemcpyDeviceToHost,
+                           s)) != cudaSuccess)
+    return fail_cuda(e, "O download");
+  return AGMM_OK;
+}
+
+agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream) {
+  (void)plan;
+  if (!workspace) return fail(AGMM_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e, "stream synchronize");
+  int words[4] = {0, 0, 0, 0};
+  if ((e = cudaMemcpy(words, workspace, sizeof words, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail_cuda(e, "status read");
+  if (words[0] == 0) return AGMM_OK;
+  if ((e = cudaMemset(workspace, 0, sizeof words)) != cudaSuccess) return fail_cuda(e, "status clear");
+  static const char* roles[] = {"?", "producer", "mma", "epilogue", "drain"};
+  const char* role = (words[1] >= 1 && words[1] <= 4) ? roles[words[1]] : roles[0];
+  return fail(words[0] == AGMM_ERR_TIMEOUT ? AGMM_ERR_TIMEOUT : AGMM_ERR_CUDA,
+              std::string("device wait ran out in the ") + role + " role (stage " + std::to_string(words[2]) +
+                  ", tile " + std::to_string(words[3]) + ")");
+}
+
+agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info) {
+  if (!plan || !info) return fail(AGMM_ERR_INVALID_ARG, "NULL argument");
+  info->path = plan->key.path;
+  info->box_rows = plan->box_rows;
+  info->chunks = plan->total_chunks;
+  info->tile_m = kTileM;
+  info->tile_n = plan->mma_n;
+  info->tile_k = kTileK;
+  info->stages = plan->stages;
+  info->splits = plan->splits;
+  info->num_tiles = plan->num_tiles;
+  info->num_ctas = (int)(plan->grid.x * plan->grid.y * plan->grid.z);
+  info->group_m = plan->group_m;
+  info->num_sms = plan->num_sms;
+  info->smem_bytes = plan->smem_bytes;
+  return AGMM_OK;
+}
+
+agmm_status_t agmm_ring_chunks(int P, int64_t m_per_device, int my_id, int box_rows, int32_t* shard,
+                               int64_t* src_row, int64_t* out_row, int32_t* valid, int64_t max_chunks,
+                               int64_t* n_chunks) {
+  if (P < 1 || P > AGMM_MAX_SHARDS || m_per_device < 1 || my_id < 0 || my_id >= P || box_rows < 1 ||
+      box_rows > 256 || !n_chunks || max_chunks < 0)
+    return fail(AGMM_ERR_INVALID_ARG, "bad ring description arguments");
+  const RingGeom g = make_ring_geom(P, m_per_device, my_id, box_rows);
+  const int64_t total = ring_total_chunks(g);
+  *n_chunks = total;
+  for (int64_t c = 0; c < total && c < max_chunks; ++c) {
+    const RingChunk ch = ring_chunk(g, c);
+    if (shard) shard[c] = ch.shard;
+    if (src_row) src_row[c] = ch.src_row;
+    if (out_row) out_row[c] = ch.out_row;
+    if (valid) valid[c] = ch.valid;
+  }
+  return AGMM_OK;
+}
+
+const char* agmm_status_string(agmm_status_t status) {
+  switch (status) {
+    case AGMM_OK: return "AGMM_OK";
+    case AGMM_ERR_INVALID_ARG: return "AGMM_ERR_INVALID_ARG";
+    case AGMM_ERR_UNSUPPORTED: return "AGMM_ERR_UNSUPPORTED";
+    case AGMM_ERR_ALIGNMENT: return "AGMM_ERR_ALIGNMENT";
+    case AGMM_ERR_CUDA: return "AGMM_ERR_CUDA";
+    case AGMM_ERR_TIMEOUT: return "AGMM_ERR_TIMEOUT";
+    case AGMM_ERR_NOMEM: return "AGMM_ERR_NOMEM";
+  }
+  return "AGMM_ERR_UNKNOWN";
+}
+
+const char* agmm_last_error(void) { return g_last_error.c_str(); }
+
+int agmm_version(void) { return AGMM_VERSION; }
+
+}  // extern "C"

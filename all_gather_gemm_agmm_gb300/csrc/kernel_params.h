@@ -1,0 +1,76 @@
+// kernel_params.h -- parameter blocks shared by the host planner
+// (agmm_api.cpp) and the sm_103a kernels (agmm_kernels.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace agmm {
+
+constexpr int kMaxShards = 8;
+constexpr int kMaxStages = 8;
+constexpr int kThreads = 192;       // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
+constexpr int kTileM = 128;         // MMA M (one CTA, 128 TMEM lanes)
+constexpr int kTileK = 64;          // k per stage: one 128-byte swizzle row of bf16
+constexpr int kASlotBytes = kTileM * kTileK * 2;  // 16 KiB
+constexpr int kStatusBytes = 256;   // status words at the start of the workspace
+
+enum Path : int { kPathRows = 0, kPathSwap = 1 };
+
+// Status word layout (int32 at the workspace base):
+//   [0] first error code (0 = none), [1] role that gave up, [2] stage, [3] tile.
+enum StatusRole : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
+
+struct __align__(64) KernelParams {
+  CUtensorMap xmap[kMaxShards];  // shard r: [m_pd, k] bf16, box {64, box_rows}, 128B swizzle
+  CUtensorMap ymap;              // Y: K-major box {64, rows} or MN-major box {64, 64}
+  void* out;                     // O [P*m_pd, n], bf16 or f32
+  int* status;                   // status words (may be null)
+  int64_t m_pd;                  // rows per shard
+  int64_t ldo;                   // row stride of O in elements (= n)
+  int P;
+  int my_id;
+  int box_rows;                  // rows per chunk
+  int total_chunks;              // chunks in the ring-ordered row sequence
+  int num_m_tiles;               // row path: 128-row tiles of chunks
+  int num_n_tiles;               // n tiles
+  int num_k_blocks;              // k / 64
+  int group_m;                   // row path: row tiles per raster group
+  int num_tiles;                 // row path: num_m_tiles * num_n_tiles
+  int stages;                    // pipeline depth (<= kMaxStages)
+  int mma_n;                     // MMA N
+  int tmem_cols;                 // TMEM columns allocated (power of two >= 32)
+  int splits;                    // swap path: k splits = cluster size
+  uint32_t b_slot_bytes;         // bytes of one B-operand stage slot (multiple of 1024)
+  uint64_t wait_limit_ns;        // bound on every mbarrier wait
+  int test_drop_first_arrive;    // test hook: producer skips its first arrival
+};
+
+struct GatherParams {
+  const uint4* src[kMaxShards];  // shard r, m_pd*k bf16
+  uint4* dst;                    // [P*m_pd, k] bf16
+  int64_t vec_per_shard;         // m_pd*k*2 / 16
+};
+
+// Kernel variant: path, Y storage (true: [n, k] -> K-major tiles), float32
+// output, and the row path's n tile (128 or 256; the swap path uses 128).
+struct KernelKey {
+  int path;
+  bool y_kmajor;
+  bool out_f32;
+  int bn;
+};
+
+// Sets the kernel's shared-memory and cluster attributes and reports how many
+// clusters of `cluster_x` CTAs can be co-resident (1-CTA clusters: CTAs/SM).
+cudaError_t prepare_agmm_kernel(const KernelKey& key, size_t smem_bytes, int cluster_x,
+                                int* max_active);
+
+cudaError_t launch_agmm_kernel(const KernelKey& key, const KernelParams& p, dim3 grid,
+                               int cluster_x, size_t smem_bytes, cudaStream_t stream);
+
+cudaError_t launch_gather_kernel(const GatherParams& g, int P, int blocks_per_shard,
+                                 cudaStream_t stream);
+
+}  // namespace agmm

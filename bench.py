@@ -1,0 +1,516 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused all-gather matmul on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--sweep]
+
+One step is one fused all-gather matmul (agmm_run) over one batch of synthetic
+inputs resident in device memory.  Timing: W untimed warm-up steps, then
+exactly K steps bracketed by a barrier and a device synchronize, on CUDA
+events recorded on the stream the kernels are launched on.  Between timed
+steps the inputs and outputs rotate over R replicas whose total footprint
+exceeds three times the L2 size, so no step reads data a previous step left
+in L2.  Rank 0 prints one JSON line.
+
+With N > 1 (torchrun) every rank runs an independent replica of the
+workload on its own GPU ("replicas only": the method's exchange is between
+shards that all live on one GPU here); value = all ranks' FLOPs / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused all-gather-GEMM TFLOP/s and % of roofline (tensor peak / HBM GB/s) on 1 GB300"
+DEFAULT_WORKLOAD = "c2_decode"
+L2_BYTES_FALLBACK = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- distributed glue
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_throughput(units_this_rank: float, seconds_this_rank: float, device=None):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    total = reduce_sum(units_this_rank, device)
+    tmax = reduce_max(seconds_this_rank, device)
+    return total / tmax, tmax
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "all_gather_gemm_agmm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (profiles/traffic_<workload>.txt)."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def gpu_uuid(device) -> str:
+    """nvidia-smi id of a torch device (its UUID; nvidia-smi ignores CUDA_VISIBLE_DEVICES)."""
+    import torch
+
+    u = str(getattr(torch.cuda.get_device_properties(device), "uuid", ""))
+    if not u:
+        return str(device.index or 0)
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def build_replicas(w, R, device, seed=1234):
+    import torch
+
+    reps = []
+    g = torch.Generator(device=device)
+    for r in range(R):
+        g.manual_seed(seed + r)
+
+        def draw(shape, std):
+            if w.dist == "uniform":
+                t = torch.rand(shape, generator=g, device=device, dtype=torch.float32) * 2 - 1
+            else:
+                t = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std
+            return t.to(torch.bfloat16)
+
+        xs = [draw((w.m_per_device, w.k), 1.0) for _ in range(w.P)]
+        y = draw((w.n, w.k) if w.rhs_transpose else (w.k, w.n), 0.02)
+        o = torch.empty((w.M, w.n), dtype=torch.bfloat16, device=device)
+        reps.append((xs, y, o))
+    return reps
+
+
+def time_graph(step_fns, K, warmup, stream):
+    """Capture one round of R steps (one per replica) in a CUDA graph, run W
+    warm-up steps, then time exactly K steps with events on `stream`."""
+    import torch
+
+    R = len(step_fns)
+    for i in range(max(warmup, 1)):
+        step_fns[i % R](stream.cuda_stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for fn in step_fns:
+            fn(stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    return graph
+
+
+def run_timed(graph, step_fns, K, stream, sampler=None):
+    import torch
+
+    R = len(step_fns)
+    full, rest = divmod(K, R)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            graph.replay()
+        for i in range(rest):
+            step_fns[i](stream.cuda_stream)
+        end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    return start.elapsed_time(end) / 1000.0, clocks
+
+
+def cpu_oracle_sample(w, target_s=8.0):
+    """The oracle as it stands, on a bounded sample of the workload's rows."""
+    import oracle
+    from all_gather_gemm_agmm_gb300.inputs import make_workload_inputs
+
+    xs, y = make_workload_inputs(w)
+    rows_total = w.M
+    lib = oracle.load()
+    # calibrate on one row, then size each call to about a second
+    t0 = time.perf_counter()
+    oracle.agmm(xs, y, w.rhs_transpose, row_begin=0, row_end=1, lib=lib)
+    t1 = max(time.perf_counter() - t0, 1e-4)
+    rows = int(max(1, min(rows_total, round(1.0 / t1))))
+    done_rows, spent, calls, r0 = 0, 0.0, 0, 0
+    while spent < target_s and calls < 200:
+        a = r0 % rows_total
+        b = min(rows_total, a + rows)
+        t0 = time.perf_counter()
+        oracle.agmm(xs, y, w.rhs_transpose, row_begin=a, row_end=b, lib=lib)
+        spent += time.perf_counter() - t0
+        done_rows += b - a
+        r0 = b
+        calls += 1
+    flops = 2.0 * done_rows * w.k * w.n
+    return {"value": flops / spent / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(lib), "kind": "oracle",
+            "sample": f"{done_rows} output rows of {w.name} ({rows_total} rows x {w.n} cols, k={w.k}) "
+                      f"in {calls} calls, {spent:.1f} s", "seconds": spent}
+
+
+def bench_ours(args, w):
+    import torch
+
+    import all_gather_gemm_agmm_gb300 as agmm
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist("nccl")
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size or L2_BYTES_FALLBACK
+    per_rep = w.unique_bytes
+    R = max(2, -(-3 * l2 // per_rep))
+    reps = build_replicas(w, R, device)
+    plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose)
+    info = plan.info()
+    ws = plan.new_workspace(False, device=device)
+    ws_unf = plan.new_workspace(True, device=device)
+    stream = torch.cuda.Stream(device=device)
+
+    def fused_step(rep):
+        xs, y, o = rep
+        xp = [x.data_ptr() for x in xs]
+        return lambda s: plan.run_ptrs(xp, y.data_ptr(), o.data_ptr(), w.my_id, ws.data_ptr(), s)
+
+    def unfused_step(rep):
+        xs, y, o = rep
+        return lambda s: plan.run_unfused(xs, y, o, w.my_id, ws_unf, s)
+
+    fused = [fused_step(r) for r in reps]
+    graph = time_graph(fused, args.steps, args.warmup, stream)
+    # estimate step time, then pick K when not given
+    est, _ = run_timed(graph, fused, R, stream)
+    K = args.steps if args.steps else int(max(R, min(500000, round(1.5 / max(est / R, 1e-7)))))
+    sampler = ClockSampler(gpu_uuid(device))
+    elapsed, clocks = run_timed(graph, fused, K, stream, sampler)
+    plan.query_status(ws, stream)
+    value, tmax = aggregate_throughput(w.flops * K / 1e12, elapsed, device)
+    ms_per_step = tmax / K * 1e3
+
+    # unfused comparison (same replicas, same method)
+    unf = [unfused_step(r) for r in reps]
+    g2 = time_graph(unf, K, args.warmup, stream)
+    K2 = max(R, min(K, int(round(1.0 / max(est / R, 1e-7)))))
+    el2, _ = run_timed(g2, unf, K2, stream)
+    plan.query_status(ws_unf, stream)
+    unf_ms = reduce_max(el2, device) / K2 * 1e3
+    del g2
+
+    # end to end through the C ABI from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        xs_h = [x.cpu().pin_memory() for x in reps[0][0]]
+        y_h = reps[0][1].cpu().pin_memory()
+        o_h = torch.empty((w.M, w.n), dtype=torch.bfloat16).pin_memory()
+        xs_d, y_d, o_d = reps[0]
+        Ke = max(3, min(K, 200 if w.unique_bytes < 1e9 else 20))
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                plan.run_host(xs_h, y_h, o_h, xs_d, y_d, o_d, w.my_id, ws, stream)
+            torch.cuda.synchronize()
+            barrier()
+            t0 = time.perf_counter()
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(Ke):
+                plan.run_host(xs_h, y_h, o_h, xs_d, y_d, o_d, w.my_id, ws, stream)
+            ev1.record(stream)
+            ev1.synchronize()
+            wall = time.perf_counter() - t0
+        e_el = max(ev0.elapsed_time(ev1) / 1000.0, wall)
+        e_val, _ = aggregate_throughput(w.flops * Ke / 1e12, e_el, device)
+        e2e = {"value": e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * (w.M * w.k + w.k * w.n),
+               "d2h_bytes_per_step": 2 * w.M * w.n, "steps": Ke, "ms_per_step": e_el / Ke * 1e3}
+
+    peaks, peak_src = load_peaks()
+    launch_s = tmax / K
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ai = w.flops / w.unique_bytes
+    if ai < ridge:
+        achieved = w.unique_bytes / launch_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = w.flops / launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])}
+    roof["traffic"] = recorded_traffic(w.name)
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["kernel"] = "agmm_fused_sm103a"
+    roof["algorithmic_bytes_per_launch"] = w.unique_bytes
+    roof["flops_per_launch"] = w.flops
+    roof["roofline_time_us"] = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.unique_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+    roof["frac_of_roofline_time"] = roof["roofline_time_us"] / (launch_s * 1e6)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_n, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded torch.Generator on device; shapes of the workload)",
+        "config": {"workload": w.name, "P": w.P, "m_per_device": w.m_per_device, "k": w.k, "n": w.n,
+                   "rhs_transpose": w.rhs_transpose, "my_id": w.my_id, "dist": w.dist,
+                   "l2": f"{R} rotating input/output replicas, {R * per_rep / 2**20:.0f} MiB > 3x L2 "
+                         f"({l2 / 2**20:.0f} MiB)",
+                   "timing": "CUDA graph of one replica round, events on the launch stream",
+                   "parallelism": f"replicas x{ws_n}", "plan": info},
+        "roofline": roof,
+        "unfused": {"ms_per_step": unf_ms, "value": w.flops / (unf_ms / 1e3) / 1e12 * ws_n, "steps": K2,
+                    "fused_speedup": unf_ms / ms_per_step},
+        "e2e": e2e,
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_oracle_sample(w, target_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def bench_sweep(args):
+    """Fused vs unfused device time at every point of the k=5120, n=2560 sweep."""
+    import torch
+
+    import all_gather_gemm_agmm_gb300 as agmm
+    from all_gather_gemm_agmm_gb300.inputs import SWEEP
+
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size or L2_BYTES_FALLBACK
+    peaks, _ = load_peaks()
+    stream = torch.cuda.Stream(device=device)
+    for w in SWEEP:
+        R = max(2, -(-3 * l2 // w.unique_bytes))
+        reps = build_replicas(w, R, device)
+        plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose)
+        ws = plan.new_workspace(False, device=device)
+        wsu = plan.new_workspace(True, device=device)
+        fused = [(lambda rep: (lambda s: plan.run(rep[0], rep[1], rep[2], w.my_id, ws, s)))(r) for r in reps]
+        unf = [(lambda rep: (lambda s: plan.run_unfused(rep[0], rep[1], rep[2], w.my_id, wsu, s)))(r) for r in reps]
+        g1 = time_graph(fused, 0, 3, stream)
+        est, _ = run_timed(g1, fused, R, stream)
+        K = int(max(R, min(100000, round(0.3 / max(est / R, 1e-7)))))
+        t1, _ = run_timed(g1, fused, K, stream)
+        g2 = time_graph(unf, 0, 3, stream)
+        t2, _ = run_timed(g2, unf, K, stream)
+        plan.query_status(ws, stream)
+        f_us, u_us = t1 / K * 1e6, t2 / K * 1e6
+        roof_us = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.unique_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+        print(json.dumps({"sweep_point": w.name, "P": w.P, "m_per_device": w.m_per_device,
+                          "rhs_transpose": w.rhs_transpose, "fused_us": f_us, "unfused_us": u_us,
+                          "fused_tflops": w.flops / (f_us * 1e-6) / 1e12, "roofline_us": roof_us,
+                          "frac_of_roofline": roof_us / f_us, "fused_faster": f_us < u_us,
+                          "plan": plan.info()}), flush=True)
+        del g1, g2, reps
+        torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------------------------------- reference arm
+def bench_reference(args, w):
+    """The oracle as it stands, on the host cores, on bounded samples of the
+    same workload: each step computes a block of output rows."""
+    ws_n, rank, _ = dist_env()
+    if ws_n > 1 and rank != 0:
+        return
+    import oracle
+    from all_gather_gemm_agmm_gb300.inputs import make_workload_inputs
+
+    xs, y = make_workload_inputs(w)
+    lib = oracle.load()
+    t0 = time.perf_counter()
+    oracle.agmm(xs, y, w.rhs_transpose, row_begin=0, row_end=1, lib=lib)
+    t_row = max(time.perf_counter() - t0, 1e-4)
+    rows = int(max(1, min(w.M, round(args.ref_step_seconds / t_row))))
+    for i in range(args.warmup):
+        oracle.agmm(xs, y, w.rhs_transpose, row_begin=0, row_end=rows, lib=lib)
+    K = args.steps or 5
+    t0 = time.perf_counter()
+    for i in range(K):
+        a = (i * rows) % max(1, w.M - rows + 1)
+        oracle.agmm(xs, y, w.rhs_transpose, row_begin=a, row_end=a + rows, lib=lib)
+    el = time.perf_counter() - t0
+    flops = 2.0 * rows * w.k * w.n * K
+    val = flops / el / 1e12
+    sample = f"{rows} of {w.M} output rows of {w.name} per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": ws_n, "steps": K,
+        "warmup": args.warmup, "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded torch.Generator on the CPU)",
+        "config": {"workload": w.name, "P": w.P, "m_per_device": w.m_per_device, "k": w.k, "n": w.n,
+                   "rhs_transpose": w.rhs_transpose, "my_id": w.my_id},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.max_threads(lib), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 1.5 s worth)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", action="store_true", help="fused vs unfused at every sweep point")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=1.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from all_gather_gemm_agmm_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        bench_reference(args, w)
+    elif args.sweep:
+        bench_sweep(args)
+    else:
+        bench_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * agmm.h -- C ABI of the GB300 (sm_103a) fused all-gather matmul.
+ *
+ * Operation (tpu_inference "all_gather_matmul.py", all_gather_matmul
+ * docstring and _all_gather_kernel; AllGather-GEMM tutorial,
+ * torch_allgather_gemm):
+ *
+ *     O = concat(X_0, ..., X_{P-1}) @ Ycan
+ *     Ycan = Y            (rhs_transpose == 0, Y stored [k, n])
+ *          = transpose(Y) (rhs_transpose != 0, Y stored [n, k])
+ *
+ * On one GPU the P "ranks" of the pages are P separate shard buffers
+ * X_r [m_per_device, k] in the same device memory.  The kernel reads them
+ * through a per-shard TMA descriptor table in the pages' bidirectional ring
+ * order (ring step s consumes the left half of shard (my_id + s) mod P and the
+ * right half of shard (my_id - s) mod P, _do_o_local_copy), accumulates in
+ * float32 in tensor memory (preferred_element_type=float32 in _do_mxu) and
+ * writes row block r of O at rows [r*m_per_device, (r+1)*m_per_device).  The
+ * gathered left-hand side is never written to device memory by agmm_run.
+ *
+ * Layout: every matrix is dense row-major bf16.  O is [P*m_per_device, n],
+ * bf16 (AGMM_BF16) or float32 (AGMM_BF16_F32OUT).
+ *
+ * Ownership: the caller owns every device buffer (shards, Y, O, workspace)
+ * and the stream.  A plan owns host memory only.
+ *
+ * Errors: every call returns a status; nothing throws across this boundary.
+ * agmm_last_error() gives a message for the last failing call of the calling
+ * thread.  Runs are asynchronous on the given stream; a device-side timeout
+ * is reported later through agmm_query_status().
+ *
+ * Threads: a plan caches tensor-map descriptors and is not safe for
+ * concurrent use from several host threads.  Distinct plans are independent.
+ */
+#ifndef AGMM_H_
+#define AGMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AGMM_VERSION 1
+#define AGMM_MAX_SHARDS 8 /* per-peer descriptor tables are capped at 8 peers
+                             (jax mosaic gpu launch_context.py, _get_tma_desc) */
+
+typedef enum {
+  AGMM_OK = 0,
+  AGMM_ERR_INVALID_ARG = 1, /* a size, index or pointer is out of range         */
+  AGMM_ERR_UNSUPPORTED = 2, /* no sm_103a device, or a shape this build rejects */
+  AGMM_ERR_ALIGNMENT = 3,   /* a device pointer is not 16-byte aligned          */
+  AGMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed                */
+  AGMM_ERR_TIMEOUT = 5,     /* a device-side wait ran past its limit            */
+  AGMM_ERR_NOMEM = 6        /* host allocation failed                           */
+} agmm_status_t;
+
+typedef enum {
+  AGMM_BF16 = 0,        /* bf16 inputs, float32 accumulation, bf16 output    */
+  AGMM_BF16_F32OUT = 1  /* bf16 inputs, float32 accumulation, float32 output */
+} agmm_dtype_t;
+
+typedef struct agmm_plan_s* agmm_plan_t;
+
+/* What the planner chose (for tests, tracing and the benchmark). */
+typedef struct {
+  int path;          /* 0: row tiles (MMA M spans gathered rows);
+                        1: swapped tiles (MMA M spans n, gathered rows are MMA N) */
+  int box_rows;      /* rows per X tensor-map box (a "chunk")                    */
+  int chunks;        /* chunks in the whole ring-ordered row sequence            */
+  int tile_m;        /* MMA M                                                    */
+  int tile_n;        /* MMA N                                                    */
+  int tile_k;        /* k elements per pipeline stage                            */
+  int stages;        /* shared-memory pipeline depth                             */
+  int splits;        /* k splits reduced inside a thread-block cluster           */
+  int num_tiles;     /* output tiles                                             */
+  int num_ctas;      /* CTAs launched by agmm_run                                */
+  int group_m;       /* row tiles per raster group                               */
+  int num_sms;       /* SMs of the planned device                                */
+  size_t smem_bytes; /* dynamic shared memory per CTA                            */
+} agmm_plan_info_t;
+
+/*
+ * agmm_plan -- validate a problem and choose tiles for the current device.
+ *
+ * Arguments follow all_gather_matmul's problem statement: P shards (the mesh
+ * axis size), m_per_device rows per shard, contraction length k, n output
+ * columns (the page's n_per_device), dtype, rhs_transpose.
+ *
+ * Accepted: 1 <= P <= 8; m_per_device >= 1; k >= 128 and k % 128 == 0;
+ * n >= 128 and n % 128 == 0 (validate_inputs' k and n rules); P*m_per_device*k,
+ * k*n and P*m_per_device*n below 2^40 elements.  validate_inputs' rules that
+ * m be a multiple of 16*P are relaxed: any m_per_device >= 1 is accepted and
+ * an odd shard is split as floor(m/2) left rows and the rest right rows.
+ *
+ * Returns AGMM_ERR_INVALID_ARG (with *out_plan = NULL) for a rejected shape,
+ * AGMM_ERR_UNSUPPORTED when the current device is not sm_103, AGMM_ERR_CUDA
+ * when no device can be queried, AGMM_ERR_NOMEM on host allocation failure.
+ * Shape validation happens before any CUDA call.
+ */
+agmm_status_t agmm_plan(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
+                        int rhs_transpose, agmm_plan_t* out_plan);
+
+/* Release a plan.  NULL is a no-op. */
+void agmm_destroy(agmm_plan_t plan);
+
+/*
+ * Bytes of device workspace agmm_run (unfused == 0) or agmm_run_unfused
+ * (unfused != 0) needs.  The first 256 bytes hold the device status words;
+ * the unfused path adds the gathered [P*m_per_device, k] bf16 buffer at
+ * offset 256.  The workspace must be zero-filled before its first use and
+ * must not be shared by runs that overlap on the device.  Returns 0 for NULL.
+ */
+size_t agmm_workspace_bytes(agmm_plan_t plan, int unfused);
+
+/*
+ * agmm_run -- the fused all-gather matmul, asynchronous on `stream`.
+ *
+ *   x_shards  host array of P device pointers; shard r is [m_per_device, k]
+ *   y         device pointer, [k, n] or (rhs_transpose) [n, k]
+ *   o         device pointer, [P*m_per_device, n]; must not overlap an input
+ *   my_id     this rank's index in [0, P): ring step 0 starts at shard my_id
+ *   workspace device pointer to agmm_workspace_bytes(plan, 0) bytes
+ *   stream    a cudaStream_t (NULL: the legacy default stream)
+ *
+ * Every device pointer must be 16-byte aligned (TMA: global addresses and
+ * strides are multiples of 16 bytes).  The result does not depend on my_id.
+ * Returns AGMM_ERR_INVALID_ARG / AGMM_ERR_ALIGNMENT for bad arguments (nothing
+ * is launched), AGMM_ERR_CUDA if the launch fails.
+ */
+agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o,
+                       int my_id, void* workspace, void* stream);
+
+/*
+ * agmm_run_unfused -- the decomposed comparison path: a gather kernel copies
+ * shard r to rows [r*m_per_device, (r+1)*m_per_device) of a scratch buffer in
+ * the workspace (the decomposed approach of the AllGather-GEMM tutorial), then
+ * the same tensor-core GEMM runs on it as a single shard.  Same arguments and
+ * result as agmm_run; workspace is agmm_workspace_bytes(plan, 1) bytes.
+ */
+agmm_status_t agmm_run_unfused(agmm_plan_t plan, const void* const* x_shards, const void* y,
+                               void* o, int my_id, void* workspace, void* stream);
+
+/*
+ * agmm_run_host -- agmm_run from host memory: copies each host shard to
+ * x_dev[r] and the host Y to y_dev, runs, and copies O back to o_host, all
+ * asynchronously on `stream` (host buffers should be pinned for overlap; the
+ * caller synchronizes before reading o_host).  Device buffers as in agmm_run.
+ */
+agmm_status_t agmm_run_host(agmm_plan_t plan, const void* const* x_host, const void* y_host,
+                            void* o_host, void* const* x_dev, void* y_dev, void* o_dev, int my_id,
+                            void* workspace, void* stream);
+
+/*
+ * Synchronize `stream`, read the device status words in `workspace` and
+ * clear them.  Returns AGMM_OK, AGMM_ERR_TIMEOUT if a kernel gave up on a
+ * wait since the last query, or AGMM_ERR_CUDA if the stream reports an error.
+ */
+agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream);
+
+/* Fill *info with the plan's choices. */
+agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info);
+
+/*
+ * The ring-ordered row sequence, host side (no device needed).  For box
+ * height box_rows the sequence is cut into chunks; chunk c covers rows
+ * [src_row[c], src_row[c] + valid[c]) of shard shard[c], which land at rows
+ * [out_row[c], out_row[c] + valid[c]) of O.  Chunks follow ring step s = 0..P-1,
+ * left half of shard (my_id+s) mod P then right half of shard (my_id-s) mod P.
+ * Writes at most max_chunks entries and stores the full count in *n_chunks.
+ */
+agmm_status_t agmm_ring_chunks(int P, int64_t m_per_device, int my_id, int box_rows,
+                               int32_t* shard, int64_t* src_row, int64_t* out_row,
+                               int32_t* valid, int64_t max_chunks, int64_t* n_chunks);
+
+/* Static description of a status code. */
+const char* agmm_status_string(agmm_status_t status);
+
+/* Detail of the calling thread's last failing call ("" if none). */
+const char* agmm_last_error(void);
+
+/* AGMM_VERSION of the loaded library. */
+int agmm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AGMM_H_ */

@@ -18,3 +18,12 @@ def oracle_lib():
     import oracle
 
     return oracle.load()
+
+
+@pytest.fixture(scope="session")
+def agmm_lib():
+    """libagmm.so, built in-tree if it is missing or stale (nvcc cross-compiles)."""
+    from all_gather_gemm_agmm_gb300 import _build, load_library
+
+    _build.build()
+    return load_library()

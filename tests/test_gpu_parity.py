@@ -1,0 +1,131 @@
+"""GPU parity: the sm_103a kernels (through the C ABI) against the CPU oracle
+on the same seeded inputs."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from all_gather_gemm_agmm_gb300.inputs import WORKLOADS, make_inputs
+
+from parity import alloc_output_guarded, check, guards_intact, oracle_rows, to_device_guarded
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def agmm():
+    import all_gather_gemm_agmm_gb300 as m
+    from all_gather_gemm_agmm_gb300 import _build
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _build.build()
+    m.load_library()
+    return m
+
+
+def _run(agmm, xs_cpu, y_cpu, rt, my_id, f32=False, unfused=False, plan=None):
+    P = len(xs_cpu)
+    m, k = xs_cpu[0].shape
+    n = y_cpu.shape[0] if rt else y_cpu.shape[1]
+    xs = [to_device_guarded(x)[0] for x in xs_cpu]
+    y, _ = to_device_guarded(y_cpu)
+    o, obuf = alloc_output_guarded(P * m, n, f32)
+    plan = plan or agmm.Plan(P, m, k, n, rt, f32)
+    ws = plan.new_workspace(unfused)
+    (plan.run_unfused if unfused else plan.run)(xs, y, o, my_id, ws)
+    plan.query_status(ws)
+    torch.cuda.synchronize()
+    assert guards_intact(obuf), "a store landed outside O"
+    return o, plan
+
+
+# Small and mid cases the oracle finishes in seconds: several tiles, ragged
+# tails, odd shards, both layouts, both paths.
+SMALL = [
+    # P, m_pd, k, n, rt, dist
+    (2, 16, 256, 128, False, "uniform"),   # the tiny uniform workload
+    (4, 64, 4096, 1024, True, "normal"),   # the decode-like workload, full size
+    (8, 8, 1024, 256, False, "normal"),
+    (3, 5, 128, 128, True, "normal"),
+    (1, 1, 128, 128, False, "normal"),
+    (2, 128, 512, 384, True, "normal"),
+    (3, 200, 512, 384, False, "normal"),   # rows path, ragged halves of 100
+    (2, 300, 256, 512, True, "normal"),    # rows path, n tile 256
+    (5, 77, 384, 256, False, "uniform"),   # rows path, odd shards
+    (8, 130, 256, 640, True, "normal"),    # rows path, n 640 = 5 x 128
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "P{}_m{}_k{}_n{}_{}".format(*c[:4], "rt" if c[4] else "nt"))
+def test_parity_small(agmm, case):
+    P, m, k, n, rt, dist = case
+    xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, dist=dist, seed=0)
+    ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+    o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=P - 1)
+    check(o, ref32, f"{case} bf16 {plan.info()}")
+    o32, _ = _run(agmm, xs_cpu, y_cpu, rt, my_id=0, f32=True)
+    check(o32, ref32, f"{case} f32")
+
+
+@pytest.mark.parametrize("case", [(3, 200, 512, 384, False), (4, 64, 1024, 256, True), (5, 9, 256, 128, False)])
+def test_result_independent_of_my_id(agmm, case):
+    P, m, k, n, rt = case
+    xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=1)
+    outs = [_run(agmm, xs_cpu, y_cpu, rt, my_id=i)[0] for i in range(P)]
+    for i in range(1, P):
+        assert torch.equal(outs[0].view(torch.int16), outs[i].view(torch.int16)), f"my_id {i} differs"
+
+
+@pytest.mark.parametrize("case", [(4, 64, 4096, 1024, True), (3, 200, 512, 384, False), (2, 300, 256, 512, True)])
+def test_unfused_matches(agmm, case):
+    P, m, k, n, rt = case
+    xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=2)
+    ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+    fused, _ = _run(agmm, xs_cpu, y_cpu, rt, my_id=1)
+    unf, _ = _run(agmm, xs_cpu, y_cpu, rt, my_id=1, unfused=True)
+    check(unf, ref32, f"{case} unfused")
+    check(fused, ref32, f"{case} fused")
+
+
+@pytest.mark.parametrize("force_rows", [True])
+def test_rows_path_on_small_m(agmm, force_rows, monkeypatch):
+    # The planner sends small problems to the swapped tiles; force the row
+    # tiles (box heights 8 and 16) to cover them too.
+    monkeypatch.setenv("AGMM_PATH", "0")
+    for (P, m, k, n, rt) in [(2, 16, 256, 128, False), (8, 8, 512, 256, True), (3, 5, 256, 256, False)]:
+        xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=3)
+        ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+        o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=P - 1)
+        assert plan.info()["path"] == 0
+        check(o, ref32, f"forced rows {P},{m}")
+
+
+def _sample_ranges(P, m, M):
+    rows = set()
+    for r in range(P):
+        for off in (0, m // 2 - 1, m // 2, m - 1):
+            if 0 <= off < m:
+                rows.add(r * m + off)
+    rng = np.random.default_rng(0)
+    rows.update(int(v) for v in rng.integers(0, M, size=24))
+    return sorted(rows)
+
+
+FULL = ["c3_mid", "c4_prefill", "sweep_P2_m1000_nt", "sweep_P8_m1000_rt", "sweep_P4_m4096_nt",
+        "sweep_P8_m32_rt", "sweep_P2_m8_nt", "sweep_P4_m128_rt", "sweep_P8_m128_nt"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_parity_full_size_sampled_rows(agmm, name):
+    w = WORKLOADS[name]
+    xs_cpu, y_cpu = make_inputs(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, w.dist, w.seed)
+    o, plan = _run(agmm, xs_cpu, y_cpu, w.rhs_transpose, my_id=w.my_id)
+    rows = _sample_ranges(w.P, w.m_per_device, w.M)
+    ref = oracle_rows(xs_cpu, y_cpu, w.rhs_transpose, rows)
+    idx = torch.tensor(rows, device=o.device)
+    check(o.index_select(0, idx), ref, f"{name} {plan.info()}")
+    # every row written (no NaN left from the poison) and finite
+    assert bool(torch.isfinite(o.float()).all())
