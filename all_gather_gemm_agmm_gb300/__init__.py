@@ -31,7 +31,7 @@ AGMM_BF16_F32OUT = 1
 EXPORTED_SYMBOLS = [
     "agmm_plan", "agmm_destroy", "agmm_workspace_bytes", "agmm_run", "agmm_run_unfused",
     "agmm_run_host", "agmm_query_status", "agmm_plan_info", "agmm_ring_chunks",
-    "agmm_status_string", "agmm_last_error", "agmm_version",
+    "agmm_status_string", "agmm_last_error", "agmm_version", "agmm_trace_bytes", "agmm_set_trace",
 ]
 
 
@@ -89,6 +89,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.agmm_last_error.restype = ctypes.c_char_p
     lib.agmm_version.argtypes = []
     lib.agmm_version.restype = c_int
+    lib.agmm_trace_bytes.argtypes = [vp]
+    lib.agmm_trace_bytes.restype = ctypes.c_size_t
+    lib.agmm_set_trace.argtypes = [vp, vp, ctypes.c_size_t]
+    lib.agmm_set_trace.restype = c_int
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -167,6 +171,20 @@ class Plan:
         inf = PlanInfo()
         _check(self._lib.agmm_plan_info(self._h, ctypes.byref(inf)))
         return {f: getattr(inf, f) for f, _ in PlanInfo._fields_}
+
+    def enable_trace(self, device=None):
+        """Allocate and attach a device trace buffer; returns it ([CTAs, 16] int64)."""
+        import torch
+
+        nbytes = int(self._lib.agmm_trace_bytes(self._h))
+        buf = torch.zeros((nbytes // 128, 16), dtype=torch.int64, device=device or "cuda")
+        _check(self._lib.agmm_set_trace(self._h, buf.data_ptr(), nbytes))
+        self._trace = buf
+        return buf
+
+    def disable_trace(self) -> None:
+        _check(self._lib.agmm_set_trace(self._h, None, 0))
+        self._trace = None
 
     def workspace_bytes(self, unfused: bool = False) -> int:
         return int(self._lib.agmm_workspace_bytes(self._h, int(bool(unfused))))

@@ -46,7 +46,6 @@ int env_int(const char* name, int dflt) {
 }
 
 constexpr int64_t kMaxElems = (int64_t)1 << 40;
-constexpr size_t kMaxDynSmem = 232448;  // 227 KiB per CTA on sm_100-class parts
 
 int pow2_ceil(int v) {
   int p = 1;
@@ -113,6 +112,8 @@ struct agmm_plan_s {
   size_t smem_bytes = 0;
   dim3 grid{1, 1, 1};
   int cluster_x = 1;
+  int full_tiles = 0, tail_tiles = 0, tail_splits = 1, num_items = 0;
+  size_t tail_bytes = 0;  // workspace bytes for tail counters and partials
   // descriptor cache: tensor maps depend only on the X and Y pointers
   bool cache_valid = false;
   const void* cache_x[kMaxShards] = {};
@@ -158,7 +159,7 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
       best_pad = pad;
     }
   }
-  const int64_t budget = (int64_t)kMaxDynSmem - 1024 - 256;
+  const int64_t budget = (int64_t)kMaxDynSmem - 1024 - kCtlBytes;
   pl->num_k_blocks = (int)(pl->k / kTileK);
   if (best_bh > 0 && force_path != kPathRows) {
     pl->key.path = kPathSwap;
@@ -173,9 +174,10 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
     pl->stages = (int)std::min<int64_t>(kMaxStages, budget / stage_bytes);
     pl->stages = std::min(pl->stages, std::max(2, env_int("AGMM_STAGES", kMaxStages)));
-    while ((int64_t)pl->stages * stage_bytes < (int64_t)pl->mma_n * kTileM * 4) ++pl->stages;
+    // Upper bound on the k splits (cluster size); plan_impl lowers it until
+    // one wave of clusters covers every n tile.
     int splits = pl->num_sms / pl->num_n_tiles;
-    splits = std::max(1, std::min(splits, std::min(8, pl->num_k_blocks)));
+    splits = std::max(1, std::min(splits, std::min(16, pl->num_k_blocks)));
     const int env_splits = env_int("AGMM_SPLITK", 0);
     if (env_splits > 0) splits = std::max(1, std::min(env_splits, std::min(16, pl->num_k_blocks)));
     pl->splits = splits;
@@ -216,7 +218,7 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->tmem_cols = 2 * bn;
     pl->group_m = std::max(1, env_int("AGMM_GROUP_M", 8));
   }
-  pl->smem_bytes = 1024 + (size_t)pl->stages * (kASlotBytes + pl->b_slot_bytes) + 256;
+  pl->smem_bytes = 1024 + (size_t)pl->stages * (kASlotBytes + pl->b_slot_bytes) + kCtlBytes;
   return AGMM_OK;
 }
 
@@ -253,26 +255,74 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
     delete pl;
     return st;
   }
-  // Attributes and co-residency: shrink the cluster until it can be scheduled.
+  // Attributes and co-residency.  Swap path: the largest cluster (k split)
+  // for which one wave of clusters covers every n tile; rows path: one
+  // persistent CTA per SM.
   for (;;) {
+    if (pl->key.path == kPathSwap) {
+      // The k-split reduction reuses the pipeline slots as its receive buffer:
+      // splits x cpo slots of 128 floats (cpo = owner columns, 16-aligned).
+      const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
+      const int64_t budget = (int64_t)kMaxDynSmem - 1024 - kCtlBytes;
+      const int64_t groups = (pl->total_chunks * (int64_t)pl->box_rows + 15) / 16;
+      const int64_t cpo = (groups + pl->splits - 1) / pl->splits * 16;
+      const int64_t recv = (int64_t)pl->splits * cpo * kTileM * 4;
+      while ((int64_t)pl->stages * stage_bytes < recv && (int64_t)(pl->stages + 1) * stage_bytes <= budget &&
+             pl->stages < kMaxStages)
+        ++pl->stages;
+      if ((int64_t)pl->stages * stage_bytes < recv) {
+        if (pl->splits <= 1) {
+          delete pl;
+          return fail(AGMM_ERR_UNSUPPORTED, "reduction buffer does not fit in shared memory");
+        }
+        --pl->splits;
+        continue;
+      }
+      pl->smem_bytes = 1024 + (size_t)pl->stages * stage_bytes + kCtlBytes;
+    }
     int active = 0;
     e = prepare_agmm_kernel(pl->key, pl->smem_bytes, pl->splits, &active);
     if (e != cudaSuccess) {
       delete pl;
       return fail_cuda(e, "kernel attribute setup");
     }
-    if (active > 0) break;
+    if (pl->splits == 1) active *= pl->num_sms;  // CTAs per SM -> CTAs per device
+    const int needed = pl->key.path == kPathSwap ? pl->num_n_tiles : 1;
+    if (active >= needed || (pl->splits == 1 && active > 0)) break;
     if (pl->splits <= 1) {
       delete pl;
       return fail(AGMM_ERR_UNSUPPORTED, "kernel cannot be resident with the planned shared memory");
     }
-    pl->splits = std::max(1, pl->splits / 2);
+    --pl->splits;
   }
   if (pl->key.path == kPathSwap) {
     pl->grid = dim3((unsigned)pl->splits, (unsigned)pl->num_n_tiles, 1);
     pl->cluster_x = pl->splits;
   } else {
-    pl->grid = dim3((unsigned)std::min(pl->num_tiles, pl->num_sms), 1, 1);
+    // Persistent CTAs, one per SM.  The last, partial wave of tiles is split
+    // along k so that it keeps every SM busy: each tail tile becomes s parts.
+    const int G = pl->num_sms;
+    const int W = pl->num_tiles / G;
+    const int R = pl->num_tiles - W * G;
+    int s_tail = 1;
+    if (R > 0) s_tail = std::max(1, std::min({G / R, 8, pl->num_k_blocks / 4}));
+    const int env_tail = env_int("AGMM_TAIL_SPLIT", -1);
+    if (env_tail >= 0 && R > 0) s_tail = std::max(1, std::min({env_tail, G / R, pl->num_k_blocks}));
+    pl->tail_splits = s_tail;
+    if (s_tail > 1) {
+      pl->full_tiles = W * G;
+      pl->tail_tiles = R;
+      pl->num_items = pl->full_tiles + R * s_tail;
+      pl->grid = dim3((unsigned)(W > 0 ? G : R * s_tail), 1, 1);
+      pl->tail_bytes = (size_t)(R * 4 + 255) / 256 * 256 +
+                       (size_t)R * (s_tail - 1) * kTileM * (size_t)pl->key.bn * 4;
+    } else {
+      pl->full_tiles = pl->num_tiles;
+      pl->tail_tiles = 0;
+      pl->num_items = pl->num_tiles;
+      pl->grid = dim3((unsigned)std::min(pl->num_tiles, G), 1, 1);
+      pl->tail_bytes = 0;
+    }
     pl->cluster_x = 1;
   }
   KernelParams& kp = pl->params;
@@ -280,6 +330,8 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.ldo = n;
   kp.P = P;
   kp.box_rows = pl->box_rows;
+  kp.box_shift = 0;
+  while ((1 << kp.box_shift) < pl->box_rows) ++kp.box_shift;
   kp.total_chunks = pl->total_chunks;
   kp.num_m_tiles = pl->num_m_tiles;
   kp.num_n_tiles = pl->num_n_tiles;
@@ -293,6 +345,9 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.b_slot_bytes = pl->b_slot_bytes;
   kp.wait_limit_ns = (uint64_t)std::max(1, env_int("AGMM_WAIT_LIMIT_MS", 2000)) * 1000000ull;
   kp.test_drop_first_arrive = env_int("AGMM_TEST_DROP_ARRIVE", 0) != 0;
+  kp.full_tiles = pl->full_tiles;
+  kp.tail_splits = pl->tail_splits;
+  kp.num_items = pl->num_items;
   if (with_sub && P > 1) {
     st = plan_impl(1, pl->M(), k, n, dtype, rhs_t, false, &pl->sub);
     if (st != AGMM_OK) {
@@ -323,8 +378,10 @@ agmm_status_t check_run_args(agmm_plan_s* pl, const void* const* xs, const void*
   return AGMM_OK;
 }
 
+// status: the device status words; tail_ws: tail_bytes of workspace for the
+// split tail tiles (counters, then partials).
 agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y, void* o, int my_id,
-                           void* ws, cudaStream_t stream) {
+                           void* status, void* tail_ws, cudaStream_t stream) {
   bool same = pl->cache_valid && pl->cache_y == y;
   for (int r = 0; same && r < pl->P; ++r) same = pl->cache_x[r] == xs[r];
   KernelParams& kp = pl->params;
@@ -351,9 +408,19 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
     pl->cache_valid = true;
   }
   kp.out = o;
-  kp.status = static_cast<int*>(ws);
+  kp.status = static_cast<int*>(status);
   kp.my_id = my_id;
-  cudaError_t e = launch_agmm_kernel(pl->key, kp, pl->grid, pl->cluster_x, pl->smem_bytes, stream);
+  if (pl->tail_splits > 1) {
+    kp.tail_flags = static_cast<int*>(tail_ws);
+    kp.tail_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(tail_ws) + (pl->tail_tiles * 4 + 255) / 256 * 256);
+  } else {
+    kp.tail_flags = nullptr;
+    kp.tail_partials = nullptr;
+  }
+  // Tail owners wait for other CTAs: a cooperative launch guarantees that
+  // every CTA of the grid is resident at once.
+  cudaError_t e = launch_agmm_kernel(pl->key, kp, pl->grid, pl->cluster_x, pl->smem_bytes,
+                                     pl->tail_splits > 1, stream);
   if (e != cudaSuccess) return fail_cuda(e, "fused kernel launch");
   return AGMM_OK;
 }
@@ -378,18 +445,22 @@ void agmm_destroy(agmm_plan_t plan) {
   delete plan;
 }
 
+namespace {
+size_t gathered_bytes(const agmm_plan_s* pl) { return ((size_t)pl->M() * (size_t)pl->k * 2 + 255) / 256 * 256; }
+}  // namespace
+
 size_t agmm_workspace_bytes(agmm_plan_t plan, int unfused) {
   if (!plan) return 0;
-  size_t b = kStatusBytes;
-  if (unfused) b += ((size_t)plan->M() * (size_t)plan->k * 2 + 255) / 256 * 256;
-  return b;
+  if (!unfused || plan->P == 1) return kStatusBytes + plan->tail_bytes;
+  return kStatusBytes + gathered_bytes(plan) + plan->sub->tail_bytes;
 }
 
 agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o, int my_id,
                        void* workspace, void* stream) {
   agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace);
   if (st != AGMM_OK) return st;
-  return launch_fused(plan, x_shards, y, o, my_id, workspace, static_cast<cudaStream_t>(stream));
+  return launch_fused(plan, x_shards, y, o, my_id, workspace, static_cast<uint8_t*>(workspace) + kStatusBytes,
+                      static_cast<cudaStream_t>(stream));
 }
 
 agmm_status_t agmm_run_unfused(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o,
@@ -397,9 +468,10 @@ agmm_status_t agmm_run_unfused(agmm_plan_t plan, const void* const* x_shards, co
   agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace);
   if (st != AGMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (plan->P == 1) return launch_fused(plan, x_shards, y, o, 0, workspace, s);
+  if (plan->P == 1)
+    return launch_fused(plan, x_shards, y, o, 0, workspace, static_cast<uint8_t*>(workspace) + kStatusBytes, s);
   uint8_t* gathered = static_cast<uint8_t*>(workspace) + kStatusBytes;
-  const size_t gbytes = (size_t)plan->M() * (size_t)plan->k * 2;
+  const size_t gbytes = gathered_bytes(plan);
   for (int r = 0; r < plan->P; ++r)
     if (overlaps(x_shards[r], (size_t)plan->m_pd * plan->k * 2, gathered, gbytes))
       return fail(AGMM_ERR_INVALID_ARG, "the workspace overlaps a shard");
@@ -412,7 +484,7 @@ agmm_status_t agmm_run_unfused(agmm_plan_t plan, const void* const* x_shards, co
   cudaError_t e = launch_gather_kernel(g, plan->P, blocks, s);
   if (e != cudaSuccess) return fail_cuda(e, "gather kernel launch");
   const void* one[1] = {gathered};
-  return launch_fused(plan->sub, one, y, o, 0, workspace, s);
+  return launch_fused(plan->sub, one, y, o, 0, workspace, gathered + gbytes, s);
 }
 
 agmm_status_t agmm_run_host(agmm_plan_t plan, const void* const* x_host, const void* y_host, void* o_host,
@@ -432,7 +504,8 @@ agmm_status_t agmm_run_host(agmm_plan_t plan, const void* const* x_host, const v
       return fail_cuda(e, "shard upload");
   if ((e = cudaMemcpyAsync(y_dev, y_host, (size_t)plan->k * plan->n * 2, cudaMemcpyHostToDevice, s)) != cudaSuccess)
     return fail_cuda(e, "Y upload");
-  st = launch_fused(plan, const_cast<const void* const*>(x_dev), y_dev, o_dev, my_id, workspace, s);
+  st = launch_fused(plan, const_cast<const void* const*>(x_dev), y_dev, o_dev, my_id, workspace,
+                    static_cast<uint8_t*>(workspace) + kStatusBytes, s);
   if (st != AGMM_OK) return st;
   if ((e = cudaMemcpyAsync(o_host, o_dev, (size_t)plan->M() * plan->n * plan->out_elem, cudaMemcpyDeviceToHost,
                            s)) != cudaSuccess)
@@ -456,6 +529,23 @@ agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream)
   return fail(words[0] == AGMM_ERR_TIMEOUT ? AGMM_ERR_TIMEOUT : AGMM_ERR_CUDA,
               std::string("device wait ran out in the ") + role + " role (stage " + std::to_string(words[2]) +
                   ", tile " + std::to_string(words[3]) + ")");
+}
+
+size_t agmm_trace_bytes(agmm_plan_t plan) {
+  if (!plan) return 0;
+  return (size_t)plan->grid.x * plan->grid.y * plan->grid.z * kTraceSlots * sizeof(uint64_t);
+}
+
+agmm_status_t agmm_set_trace(agmm_plan_t plan, void* trace, size_t bytes) {
+  if (!plan) return fail(AGMM_ERR_INVALID_ARG, "plan is NULL");
+  if (trace == nullptr) {
+    plan->params.trace = nullptr;
+    return AGMM_OK;
+  }
+  if (bytes < agmm_trace_bytes(plan)) return fail(AGMM_ERR_INVALID_ARG, "trace buffer too small");
+  if ((reinterpret_cast<uintptr_t>(trace) & 7u) != 0) return fail(AGMM_ERR_ALIGNMENT, "trace buffer not 8-byte aligned");
+  plan->params.trace = static_cast<uint64_t*>(trace);
+  return AGMM_OK;
 }
 
 agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info) {

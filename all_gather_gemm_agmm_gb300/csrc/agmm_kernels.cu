@@ -36,7 +36,6 @@
 namespace agmm {
 namespace {
 
-constexpr int kCtlBytes = 256;  // barriers + flags after the stage slots
 constexpr int kStatusTimeout = 5;  // AGMM_ERR_TIMEOUT
 
 // Offsets inside the control block.
@@ -55,6 +54,8 @@ __device__ __forceinline__ uint32_t bar_drain(uint32_t ctl) {
 }
 constexpr int kAbortOffset = 8 * (2 * kMaxStages + 5);  // int
 constexpr int kTmemOffset = kAbortOffset + 16;          // uint32
+constexpr int kChunkTabOffset = 256;                    // int4[kMaxSwapChunks]: shard, src_row, valid, out_row
+static_assert(kChunkTabOffset + kMaxSwapChunks * 16 <= kCtlBytes, "control block too small");
 
 enum WaitResult : int { kWaitOk = 1, kWaitTimeout = 0, kWaitAborted = -1 };
 
@@ -94,6 +95,18 @@ __device__ __noinline__ void record_failure(const KernelParams& p, volatile int*
   }
 }
 
+// Opt-in device trace: %globaltimer stamps per CTA (16 slots of u64).
+__device__ __forceinline__ void trace(const KernelParams& p, int slot) {
+  if (p.trace != nullptr && (threadIdx.x & 31) == 0) {
+    const uint32_t cta = blockIdx.x + gridDim.x * blockIdx.y;
+    p.trace[(size_t)cta * kTraceSlots + slot] = ptx::globaltimer_ns();
+  }
+}
+
+__device__ __forceinline__ uint32_t lane_base_of(uint32_t tmem_base, int warp) {
+  return tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
+}
+
 // Row-path tile order: ring-ordered row tiles, grouped by group_m so that a
 // wave of CTAs shares a band of X rows and sweeps n inside it (L2 reuse).
 __device__ __forceinline__ void decode_row_tile(const KernelParams& p, int tile, int& mt, int& nt) {
@@ -104,6 +117,47 @@ __device__ __forceinline__ void decode_row_tile(const KernelParams& p, int tile,
   const int r = tile - grp * per_group;
   mt = first_m + r % gm;
   nt = r / gm;
+}
+
+struct WorkItem {
+  int mt, nt;    // row tile, n tile
+  int kb0, kb1;  // k blocks [kb0, kb1)
+  int part;      // part of a split tail tile (0 = owner)
+  int nparts;    // 1 for a whole tile
+  int tail;      // index of the tail tile, -1 for a whole tile
+};
+
+__device__ __forceinline__ WorkItem decode_rows_item(const KernelParams& p, int item) {
+  WorkItem w;
+  int tile;
+  if (item < p.full_tiles) {
+    tile = item;
+    w.part = 0;
+    w.nparts = 1;
+    w.tail = -1;
+    w.kb0 = 0;
+    w.kb1 = p.num_k_blocks;
+  } else {
+    const int j = item - p.full_tiles;
+    w.tail = j / p.tail_splits;
+    w.part = j - w.tail * p.tail_splits;
+    w.nparts = p.tail_splits;
+    tile = p.full_tiles + w.tail;
+    w.kb0 = (int)((int64_t)w.part * p.num_k_blocks / w.nparts);
+    w.kb1 = (int)((int64_t)(w.part + 1) * p.num_k_blocks / w.nparts);
+  }
+  decode_row_tile(p, tile, w.mt, w.nt);
+  return w;
+}
+
+__device__ __forceinline__ void epilogue_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -128,6 +182,16 @@ __device__ __forceinline__ void store_row32(void* out, int64_t ldo, int64_t row,
                           pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
                           pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
     }
+  }
+}
+
+// Store one value.
+template <bool kF32>
+__device__ __forceinline__ void store_one(void* out, int64_t ldo, int64_t row, int64_t col, float v) {
+  if constexpr (kF32) {
+    static_cast<float*>(out)[row * ldo + col] = v;
+  } else {
+    static_cast<__nv_bfloat16*>(out)[row * ldo + col] = __float2bfloat16_rn(v);
   }
 }
 
@@ -161,12 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   uint8_t* ctl_ptr = base_ptr + (ctl - base);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl_ptr + kAbortOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl_ptr + kTmemOffset);
+  int4* chunk_tab = reinterpret_cast<int4*>(ctl_ptr + kChunkTabOffset);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const RingGeom geom = make_ring_geom(p.P, p.m_pd, p.my_id, p.box_rows);
   const uint64_t limit = p.wait_limit_ns;
 
+  if (warp == 0) trace(p, 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar_full(ctl, s), 1);
@@ -184,6 +250,14 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     for (int r = 0; r < p.P; ++r) ptx::prefetch_tensormap(&p.xmap[r]);
     ptx::prefetch_tensormap(&p.ymap);
   }
+  if constexpr (kPath == kPathSwap) {
+    // The ring-ordered chunk table, computed once per CTA (the swap path keeps
+    // every chunk of the gathered LHS in one MMA N).
+    if (warp == 2 && lane < p.total_chunks) {
+      const RingChunk ch = ring_chunk(geom, lane);
+      chunk_tab[lane] = make_int4(ch.shard, (int)ch.src_row, ch.valid, (int)ch.out_row);
+    }
+  }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), (uint32_t)p.tmem_cols);
     ptx::tmem_relinquish();
@@ -192,6 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (warp == 0) {
+    trace(p, 1);
+    if (p.trace != nullptr && lane == 0) {
+      const uint32_t cta = blockIdx.x + gridDim.x * blockIdx.y;
+      p.trace[(size_t)cta * kTraceSlots + 12] = ptx::smid();
+      p.trace[(size_t)cta * kTraceSlots + 13] = ptx::cluster_ctarank();
+    }
+  }
 
   // Work of this CTA.  Rows path: tiles blockIdx.x, +gridDim.x, ...
   // Swap path: n tile blockIdx.y, k split blockIdx.x (= rank in the cluster).
@@ -202,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       (kPath == kPathSwap) ? (int)((int64_t)(split + 1) * p.num_k_blocks / p.splits) : p.num_k_blocks;
   const int tile_first = (kPath == kPathSwap) ? 0 : (int)blockIdx.x;
   const int tile_step = (kPath == kPathSwap) ? 1 : (int)gridDim.x;
-  const int tile_count = (kPath == kPathSwap) ? 1 : p.num_tiles;
+  const int tile_count = (kPath == kPathSwap) ? 1 : p.num_items;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -212,15 +294,21 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       uint32_t armed = 0, armed_parity = 0;
       bool dropped = false;
       bool ok = true;
+      bool traced_first = false;
       const int cpt = kTileM / p.box_rows;
       for (int tile = tile_first; ok && tile < tile_count; tile += tile_step) {
         int mt = 0, nt = swap_nt;
+        int kb0 = kb_begin, kb1 = kb_end;
         int shard_j[16];
         int row_j[16];
         int nchunks = 0;
         uint32_t bytes;
         if constexpr (kPath == kPathRows) {
-          decode_row_tile(p, tile, mt, nt);
+          const WorkItem wi = decode_rows_item(p, tile);
+          mt = wi.mt;
+          nt = wi.nt;
+          kb0 = wi.kb0;
+          kb1 = wi.kb1;
           for (int j = 0; j < cpt; ++j) {
             const int64_t gc = (int64_t)mt * cpt + j;
             if (gc < p.total_chunks) {
@@ -234,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         } else {
           bytes = (uint32_t)kASlotBytes + (uint32_t)p.total_chunks * p.box_rows * 128u;
         }
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           const int res = wait_phase(bar_empty(ctl, stage), phase ^ 1u, abort_flag, limit);
           if (res != kWaitOk) {
             record_failure(p, abort_flag, res, kRoleProducer, stage, tile);
@@ -270,12 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
                 for (int a = 0; a < kTileM / 64; ++a)
                   ptx::tma_load_2d(a_dst + (uint32_t)a * 8192u, &p.ymap, full, nt * kTileM + a * 64, k0);
               }
+              const uint32_t chunk_bytes = (uint32_t)p.box_rows * 128u;
               for (int c = 0; c < p.total_chunks; ++c) {
-                const RingChunk ch = ring_chunk(geom, c);
-                ptx::tma_load_2d(b_dst + (uint32_t)c * p.box_rows * 128u, &p.xmap[ch.shard], full, k0,
-                                 (int)ch.src_row);
+                const int4 e = chunk_tab[c];
+                ptx::tma_load_2d(b_dst + (uint32_t)c * chunk_bytes, &p.xmap[e.x], full, k0, e.y);
               }
             }
+          }
+          if (!traced_first) {
+            trace(p, 2);
+            traced_first = true;
           }
           if (++stage == S) {
             stage = 0;
@@ -283,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           }
         }
       }
+      trace(p, 3);
       // Wait for this thread's TMA loads still in flight (only on an abort can
       // a load be unconsumed; a consumed stage's phase has already completed).
       for (int s = 0; s < S; ++s)
@@ -313,7 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * mma_n);
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
+        int kb0 = kb_begin, kb1 = kb_end;
+        if constexpr (kPath == kPathRows) {
+          const WorkItem wi = decode_rows_item(p, tile);
+          kb0 = wi.kb0;
+          kb1 = wi.kb1;
+        }
+        for (int kb = kb0; kb < kb1; ++kb) {
           res = wait_phase(bar_full(ctl, stage), phase, abort_flag, limit);
           if (res != kWaitOk) {
             record_failure(p, abort_flag, res, kRoleMma, stage, tile);
@@ -321,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             break;
           }
           ptx::tc_fence_after();
+          if (it == 0 && kb == kb0) trace(p, 4);
           const uint32_t a_addr = a0 + (uint32_t)stage * kASlotBytes;
           const uint32_t b_addr = b0 + (uint32_t)stage * p.b_slot_bytes;
 #pragma unroll
@@ -333,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             const uint64_t b_desc =
                 b_mn ? ptx::smem_desc_sw128(b_addr + kk * 2048u, 8192u, 1024u)
                      : ptx::smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
-            ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
+            ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit(bar_empty(ctl, stage));  // frees the stage once these MMAs finish
           if (++stage == S) {
@@ -344,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         if (!ok) break;
         ptx::mma_commit(bar_acc_full(ctl, acc));  // accumulator ready for the epilogue
       }
+      trace(p, 5);
       // Every MMA this thread issued has finished once the drain barrier fires.
       ptx::mma_commit(bar_drain(ctl));
       if (!wait_drain(bar_drain(ctl), 0, limit))
@@ -368,9 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           break;
         }
         ptx::tc_fence_after();
-        int mt, nt;
-        decode_row_tile(p, tile, mt, nt);
-        const int64_t gc = (int64_t)mt * cpt + trow / p.box_rows;
+        if (it == 0) trace(p, 6);
+        const WorkItem wi = decode_rows_item(p, tile);
+        const int64_t gc = (int64_t)wi.mt * cpt + trow / p.box_rows;
         const int r = trow % p.box_rows;
         int64_t out_row = -1;
         if (gc < p.total_chunks) {
@@ -378,6 +479,27 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           if (r < ch.valid) out_row = ch.out_row + r;
         }
         const uint32_t tbase = lane_base + (uint32_t)(acc * kBN);
+        // Partial slots of this tail tile: [part-1][BN/32][128 rows][32 floats].
+        const size_t slot_floats = (size_t)kTileM * kBN;
+        float* tail_base = (wi.tail >= 0)
+                               ? p.tail_partials + (size_t)wi.tail * (wi.nparts - 1) * slot_floats
+                               : nullptr;
+        if (wi.nparts > 1 && wi.part == 0) {
+          // Owner: wait (bounded) until the other parts have published.
+          int wres = kWaitOk;
+          if (threadIdx.x == 64) {
+            const int* flag = p.tail_flags + wi.tail;
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (ld_acquire_gpu(flag) < wi.nparts - 1) {
+              if (*abort_flag) { wres = kWaitAborted; break; }
+              if (ptx::globaltimer_ns() - t0 > limit) { wres = kWaitTimeout; break; }
+              __nanosleep(64);
+            }
+            if (wres == kWaitOk) *const_cast<volatile int*>(flag) = 0;  // ready for the next run
+            else record_failure(p, abort_flag, wres, kRoleEpilogue, -2, wi.tail);
+          }
+          epilogue_bar_sync();
+        }
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
@@ -387,12 +509,41 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_acc_empty(ctl, acc));  // TMEM buffer may be reused
           }
-          if (out_row >= 0) store_row32<kF32>(p.out, p.ldo, out_row, (int64_t)nt * kBN + c * 32, v);
+          const size_t row_off = ((size_t)c * kTileM + trow) * 32;
+          if (wi.nparts > 1 && wi.part > 0) {
+            float4* dst = reinterpret_cast<float4*>(tail_base + (size_t)(wi.part - 1) * slot_floats + row_off);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          } else {
+            if (wi.nparts > 1) {
+              // own partial + part 1 + part 2 + ... in this fixed order
+              for (int pp = 1; pp < wi.nparts; ++pp) {
+                const float4* src = reinterpret_cast<const float4*>(tail_base + (size_t)(pp - 1) * slot_floats + row_off);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 q4 = __ldcg(src + i);
+                  v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) + q4.x);
+                  v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + q4.y);
+                  v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + q4.z);
+                  v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + q4.w);
+                }
+              }
+            }
+            if (out_row >= 0) store_row32<kF32>(p.out, p.ldo, out_row, (int64_t)wi.nt * kBN + c * 32, v);
+          }
+        }
+        if (wi.nparts > 1 && wi.part > 0) {
+          // Publish: every thread's stores, then one arrival for the tile.
+          __threadfence();
+          epilogue_bar_sync();
+          if (threadIdx.x == 64) atomicAdd(p.tail_flags + wi.tail, 1);
         }
       }
+      trace(p, 7);
     } else {
-      // Swap path, part 1: this CTA's float32 partial [n 128][rows mma_n] goes
-      // from TMEM into shared memory as red[col][128] (col = gathered-row slot).
+      // Swap path: wait for this CTA's float32 partial [n 128][row slots].
       int res = kWaitOk;
       if (lane == 0) res = wait_phase(bar_acc_full(ctl, 0), 0, abort_flag, limit);
       res = __shfl_sync(0xffffffffu, res, 0);
@@ -400,58 +551,117 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         if (lane == 0) record_failure(p, abort_flag, res, kRoleEpilogue, 0, swap_nt);
       } else {
         ptx::tc_fence_after();
-        float* red = reinterpret_cast<float*>(base_ptr);
-#pragma unroll 1
-        for (int cb = 0; cb < p.mma_n / 32; ++cb) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(lane_base + (uint32_t)(cb * 32), v);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) red[(cb * 32 + i) * kTileM + trow] = __uint_as_float(v[i]);
-        }
-        ptx::tc_fence_before();
+        trace(p, 6);
       }
     }
   }
 
   if constexpr (kPath == kPathSwap) {
-    // Part 2: rank `split` of the cluster owns gathered-row slots [c0, c1) and
-    // sums every rank's partial for them in rank order 0..splits-1.
+    // Reduction of the k splits.  Owner ranks hold groups of 16 gathered-row
+    // slots: rank o owns slots [o*cpo, (o+1)*cpo), cpo a multiple of 16.  In
+    // the owner's shared memory recv[r][lq][lane][4] holds rank r's partial of
+    // its slots 4*lq..4*lq+3 for one TMEM lane (one n column).  Ranks push their
+    // partials with 16-byte remote stores once every CTA's pipeline memory is
+    // idle (barrier 1); after barrier 2 each owner sums recv[0..splits-1] in
+    // rank order, so the result does not depend on timing.  With one split the
+    // CTA is its own owner.
+    const int ncols = p.total_chunks * p.box_rows;
+    const int S = p.splits;
+    const int groups = (ncols + 15) >> 4;
+    const int cpo = ((groups + S - 1) / S) * 16;
+    const uint32_t quad_bytes = (uint32_t)kTileM * 16u;  // one [lane][4] block
     __syncwarp();
-    if (p.splits > 1) ptx::cluster_sync_all(); else __syncthreads();
-    if (warp >= 2 && !*abort_flag) {
-      const int tid = threadIdx.x - 64;
-      const int lane4 = (tid & 31) * 4;
-      const int ncols = p.total_chunks * p.box_rows;
-      const int c0 = (int)((int64_t)split * ncols / p.splits);
-      const int c1 = (int)((int64_t)(split + 1) * ncols / p.splits);
-      const uint32_t red_addr = base;
-      const float* red = reinterpret_cast<const float*>(base_ptr);
-      for (int col = c0 + (tid >> 5); col < c1; col += 4) {
-        const int chunk = col / p.box_rows;
-        const int r = col - chunk * p.box_rows;
-        const RingChunk ch = ring_chunk(geom, chunk);
-        if (r >= ch.valid) continue;
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        const uint32_t off = (uint32_t)((col * kTileM + lane4) * 4);
-        if (p.splits > 1) {
-          for (int rk = 0; rk < p.splits; ++rk) {
-            const float4 v = ptx::ld_shared_cluster_v4(ptx::map_shared_rank(red_addr + off, (uint32_t)rk));
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
+    if (S > 1) ptx::cluster_sync_all();  // 1: all CTAs have drained their main loop
+    trace(p, 8);
+    if (warp >= 2) {
+      const uint32_t lane_off = (uint32_t)(((warp & 3) * 32 + lane) * 16);
+      const uint32_t my_slot0 = base + (uint32_t)(split * (cpo >> 2)) * quad_bytes + lane_off;
+      const uint32_t tbase = lane_base_of(tmem_base, warp);
+      // Two 16-column groups per round: both TMEM loads in flight, then
+      // straight-line stores (each group belongs to a single owner).  Each
+      // rank starts at its own owner's groups, so the ranks of a cluster write
+      // to different owners at any moment instead of all to the same one.
+      const int gpo = cpo >> 4;  // groups per owner
+      const int g_start = (split * gpo) % groups;
+#pragma unroll 1
+      for (int gi = 0; gi < groups; gi += 2) {
+        uint32_t v[2][16];
+        int gsel[2];
+        gsel[0] = g_start + gi;
+        if (gsel[0] >= groups) gsel[0] -= groups;
+        gsel[1] = gsel[0] + 1;
+        if (gsel[1] >= groups) gsel[1] -= groups;
+        ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(gsel[0] * 16), v[0]);
+        if (gi + 1 < groups) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(gsel[1] * 16), v[1]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (gi + h < groups) {
+            const int col0 = gsel[h] * 16;
+            const int o = col0 / cpo;
+            const uint32_t la = my_slot0 + (uint32_t)((col0 - o * cpo) >> 2) * quad_bytes;
+            if (S > 1) {
+              const uint32_t ra = ptx::map_shared_rank(la, (uint32_t)o);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                ptx::st_shared_cluster_v4(ra + q4 * quad_bytes, v[h][4 * q4], v[h][4 * q4 + 1], v[h][4 * q4 + 2],
+                                          v[h][4 * q4 + 3]);
+            } else {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                ptx::st_shared_v4(la + q4 * quad_bytes, v[h][4 * q4], v[h][4 * q4 + 1], v[h][4 * q4 + 2],
+                                  v[h][4 * q4 + 3]);
+            }
           }
-        } else {
-          s = *reinterpret_cast<const float4*>(red + col * kTileM + lane4);
         }
-        store_row4<kF32>(p.out, p.ldo, ch.out_row + r, (int64_t)swap_nt * kTileM + lane4, s);
+      }
+      ptx::tc_fence_before();
+    }
+    __syncwarp();
+    if (S > 1) ptx::cluster_sync_all(); else __syncthreads();  // 2: partials delivered
+    trace(p, 9);
+    if (warp >= 2 && !*abort_flag) {
+      // Thread t sums lane t (n column swap_nt*128 + t) of four slots at a time.
+      const int t = threadIdx.x - 64;
+      const int c0 = split * cpo;
+      const int c1 = min(ncols, c0 + cpo);
+      const float4* recv = reinterpret_cast<const float4*>(base_ptr);
+      const int qpo = cpo >> 2;  // quads per owner slot range
+      const int64_t ncol = (int64_t)swap_nt * kTileM + t;
+      for (int c = c0; c < c1; c += 4) {
+        const int lq = (c - c0) >> 2;
+        // Issue every rank's load first (independent), then add in rank order.
+        float4 part[kMaxSplits];
+#pragma unroll
+        for (int rk = 0; rk < kMaxSplits; ++rk)
+          if (rk < S) part[rk] = recv[((size_t)(rk * qpo + lq)) * kTileM + t];
+        float4 sum = part[0];
+#pragma unroll
+        for (int rk = 1; rk < kMaxSplits; ++rk) {
+          if (rk < S) {
+            sum.x += part[rk].x;
+            sum.y += part[rk].y;
+            sum.z += part[rk].z;
+            sum.w += part[rk].w;
+          }
+        }
+        const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int cj = c + j;
+          if (cj < c1) {
+            const int4 e = chunk_tab[cj >> p.box_shift];
+            const int r = cj & (p.box_rows - 1);
+            if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j]);
+          }
+        }
       }
     }
-    if (p.splits > 1) ptx::cluster_sync_all();  // keep shared memory alive for remote readers
+    trace(p, 10);
   }
 
   __syncthreads();
+  if (warp == 0) trace(p, 11);
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
@@ -502,7 +712,10 @@ cudaError_t prepare_agmm_kernel(const KernelKey& key, size_t smem_bytes, int clu
                                 int* max_active) {
   KernelFn fn = select_kernel(key);
   if (!fn) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+  // Always the device maximum: plans of different sizes share a kernel, and a
+  // later plan must never lower the limit an earlier plan launches with.
+  if (smem_bytes > kMaxDynSmem) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem);
   if (e != cudaSuccess) return e;
   if (cluster_x > 8) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -530,7 +743,7 @@ cudaError_t prepare_agmm_kernel(const KernelKey& key, size_t smem_bytes, int clu
 }
 
 cudaError_t launch_agmm_kernel(const KernelKey& key, const KernelParams& p, dim3 grid, int cluster_x,
-                               size_t smem_bytes, cudaStream_t stream) {
+                               size_t smem_bytes, bool cooperative, cudaStream_t stream) {
   KernelFn fn = select_kernel(key);
   if (!fn) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -538,15 +751,22 @@ cudaError_t launch_agmm_kernel(const KernelKey& key, const KernelParams& p, dim3
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
   if (cluster_x > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cluster_x;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster_x;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (cooperative) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, fn, p);
 }
 

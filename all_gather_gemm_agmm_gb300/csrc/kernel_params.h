@@ -15,6 +15,10 @@ constexpr int kTileM = 128;         // MMA M (one CTA, 128 TMEM lanes)
 constexpr int kTileK = 64;          // k per stage: one 128-byte swizzle row of bf16
 constexpr int kASlotBytes = kTileM * kTileK * 2;  // 16 KiB
 constexpr int kStatusBytes = 256;   // status words at the start of the workspace
+constexpr int kTraceSlots = 16;     // u64 %globaltimer stamps per CTA in the optional trace
+constexpr int kCtlBytes = 1024;     // per-CTA control block: barriers, flags, swap-path chunk table
+constexpr int kMaxSwapChunks = 32;  // swap path: at most 256 rows in chunks of >= 8 rows
+constexpr int kMaxSplits = 16;      // swap path: largest cluster (non-portable size 16)
 
 enum Path : int { kPathRows = 0, kPathSwap = 1 };
 
@@ -31,7 +35,8 @@ struct __align__(64) KernelParams {
   int64_t ldo;                   // row stride of O in elements (= n)
   int P;
   int my_id;
-  int box_rows;                  // rows per chunk
+  int box_rows;                  // rows per chunk (a power of two, 8..128)
+  int box_shift;                 // log2(box_rows)
   int total_chunks;              // chunks in the ring-ordered row sequence
   int num_m_tiles;               // row path: 128-row tiles of chunks
   int num_n_tiles;               // n tiles
@@ -45,6 +50,18 @@ struct __align__(64) KernelParams {
   uint32_t b_slot_bytes;         // bytes of one B-operand stage slot (multiple of 1024)
   uint64_t wait_limit_ns;        // bound on every mbarrier wait
   int test_drop_first_arrive;    // test hook: producer skips its first arrival
+  uint64_t* trace;               // optional [CTAs][kTraceSlots] timestamps (null: off)
+  // Rows path work items: tiles [0, full_tiles) whole, then each of the
+  // remaining (tail) tiles split into tail_splits k-ranges.  Part 0 of a
+  // tail tile owns it: the other parts leave float32 partials in
+  // tail_partials and count themselves in tail_flags[tail]; the owner waits
+  // for tail_splits-1 arrivals, adds the partials in part order and resets the
+  // counter to 0.
+  int full_tiles;
+  int tail_splits;
+  int num_items;
+  int* tail_flags;               // [tail tiles] arrival counters (zero between runs)
+  float* tail_partials;          // [tail tiles][tail_splits-1][BN/32][128][32]
 };
 
 struct GatherParams {
@@ -62,13 +79,17 @@ struct KernelKey {
   int bn;
 };
 
+// Largest dynamic shared memory a CTA may request (227 KiB on sm_100-class parts).
+constexpr size_t kMaxDynSmem = 232448;
+
 // Sets the kernel's shared-memory and cluster attributes and reports how many
 // clusters of `cluster_x` CTAs can be co-resident (1-CTA clusters: CTAs/SM).
 cudaError_t prepare_agmm_kernel(const KernelKey& key, size_t smem_bytes, int cluster_x,
                                 int* max_active);
 
 cudaError_t launch_agmm_kernel(const KernelKey& key, const KernelParams& p, dim3 grid,
-                               int cluster_x, size_t smem_bytes, cudaStream_t stream);
+                               int cluster_x, size_t smem_bytes, bool cooperative,
+                               cudaStream_t stream);
 
 cudaError_t launch_gather_kernel(const GatherParams& g, int P, int blocks_per_shard,
                                  cudaStream_t stream);

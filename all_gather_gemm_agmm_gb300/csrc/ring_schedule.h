@@ -63,19 +63,23 @@ AGMM_HD int64_t ring_total_chunks(const RingGeom& g) {
   return (int64_t)g.P * (g.chunks_l + g.chunks_r);
 }
 
-// Chunk c of the ring-ordered sequence (0 <= c < ring_total_chunks(g)).
-AGMM_HD RingChunk ring_chunk(const RingGeom& g, int64_t c) {
+// Chunk c of the ring-ordered sequence (0 <= c < ring_total_chunks(g) < 2^31;
+// 32-bit index arithmetic keeps this cheap on the device).
+AGMM_HD RingChunk ring_chunk(const RingGeom& g, int64_t c64) {
+  const int c = (int)c64;
   const int per_step = g.chunks_l + g.chunks_r;
-  const int s = (int)(c / per_step);
-  const int w = (int)(c - (int64_t)s * per_step);
+  const int s = c / per_step;
+  const int w = c - s * per_step;
   RingChunk ch;
   int64_t seg_end;
   if (w < g.chunks_l) {
-    ch.shard = (g.my_id + s) % g.P;
+    ch.shard = g.my_id + s;
+    if (ch.shard >= g.P) ch.shard -= g.P;
     ch.src_row = (int64_t)w * g.box_rows;
     seg_end = g.half_l;
   } else {
-    ch.shard = (g.my_id - s % g.P + g.P) % g.P;
+    ch.shard = g.my_id - s;
+    if (ch.shard < 0) ch.shard += g.P;
     ch.src_row = g.half_l + (int64_t)(w - g.chunks_l) * g.box_rows;
     seg_end = g.m_pd;
   }

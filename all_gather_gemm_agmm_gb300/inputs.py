@@ -74,6 +74,9 @@ WORKLOADS = {
     "c2_decode": Workload("c2_decode", 4, 64, 4096, 1024, True, 1),
     "c3_mid": Workload("c3_mid", 8, 256, 8192, 3584, False, 3),
     "c4_prefill": Workload("c4_prefill", 8, 2048, 8192, 7168, True, 5),
+    # the prefill workload with a quarter of its rows: small enough for a
+    # full ncu capture of the row-tile kernel, still larger than L2
+    "c4_quarter": Workload("c4_quarter", 8, 512, 8192, 7168, True, 5),
 }
 SWEEP = _sweep()
 for _w in SWEEP:

@@ -268,10 +268,11 @@ def cpu_oracle_sample(w, target_s=8.0):
     xs, y = make_workload_inputs(w)
     rows_total = w.M
     lib = oracle.load()
-    # calibrate on one row, then size each call to about a second
+    # calibrate on a block of rows, then size each call to about a second
+    cal = min(rows_total, 32)
     t0 = time.perf_counter()
-    oracle.agmm(xs, y, w.rhs_transpose, row_begin=0, row_end=1, lib=lib)
-    t1 = max(time.perf_counter() - t0, 1e-4)
+    oracle.agmm(xs, y, w.rhs_transpose, row_begin=0, row_end=cal, lib=lib)
+    t1 = max(time.perf_counter() - t0, 1e-4) / cal
     rows = int(max(1, min(rows_total, round(1.0 / t1))))
     done_rows, spent, calls, r0 = 0, 0.0, 0, 0
     while spent < target_s and calls < 200:
@@ -458,9 +459,10 @@ def bench_reference(args, w):
 
     xs, y = make_workload_inputs(w)
     lib = oracle.load()
+    cal = min(w.M, 32)
     t0 = time.perf_counter()
-    oracle.agmm(xs, y, w.rhs_transpose, row_begin=0, row_end=1, lib=lib)
-    t_row = max(time.perf_counter() - t0, 1e-4)
+    oracle.agmm(xs, y, w.rhs_transpose, row_begin=0, row_end=cal, lib=lib)
+    t_row = max(time.perf_counter() - t0, 1e-4) / cal
     rows = int(max(1, min(w.M, round(args.ref_step_seconds / t_row))))
     for i in range(args.warmup):
         oracle.agmm(xs, y, w.rhs_transpose, row_begin=0, row_end=rows, lib=lib)

@@ -159,6 +159,20 @@ agmm_status_t agmm_run_host(agmm_plan_t plan, const void* const* x_host, const v
  */
 agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream);
 
+/*
+ * Optional device trace: after agmm_set_trace(plan, buf, bytes) every
+ * agmm_run of this plan writes, per CTA, 16 unsigned 64-bit slots to the
+ * device buffer `buf` (agmm_trace_bytes(plan) bytes, 8-byte aligned): %globaltimer
+ * nanoseconds at kernel entry (0), after set-up (1), first and last TMA issue
+ * (2, 3), first operand arrival at the MMA thread (4), last MMA commit (5),
+ * first accumulator seen by the epilogue (6), rows-path epilogue done (7),
+ * swap-path reduction barriers (8, 9), reduction stored (10), exit (11), plus
+ * the SM id (12) and cluster rank (13).  Pass NULL to switch it off.  The
+ * buffer stays owned by the caller and must outlive the runs that use it.
+ */
+size_t agmm_trace_bytes(agmm_plan_t plan);
+agmm_status_t agmm_set_trace(agmm_plan_t plan, void* trace, size_t bytes);
+
 /* Fill *info with the plan's choices. */
 agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info);
 

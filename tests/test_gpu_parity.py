@@ -129,3 +129,18 @@ def test_parity_full_size_sampled_rows(agmm, name):
     check(o.index_select(0, idx), ref, f"{name} {plan.info()}")
     # every row written (no NaN left from the poison) and finite
     assert bool(torch.isfinite(o.float()).all())
+
+
+@pytest.mark.parametrize("tail", ["1", "2", "3", "8"])
+def test_tail_split_parts(agmm, tail, monkeypatch):
+    # The last partial wave of row tiles is split along k into parts whose
+    # float32 partials the owning part adds in a fixed order.
+    monkeypatch.setenv("AGMM_TAIL_SPLIT", tail)
+    for (P, m, k, n, rt) in [(5, 77, 1024, 256, False), (3, 200, 2048, 384, True)]:
+        xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=4)
+        ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+        o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=1)
+        check(o, ref32, f"tail split {tail} {plan.info()}")
+        # a second run reuses the zeroed counters
+        o2, _ = _run(agmm, xs_cpu, y_cpu, rt, my_id=1, plan=plan)
+        assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
