@@ -106,13 +106,14 @@ struct agmm_plan_s {
   int device = 0;
   int num_sms = 0;
   KernelKey key{};
-  int box_rows = 0, total_chunks = 0, num_m_tiles = 0, num_n_tiles = 0, num_k_blocks = 0;
+  int box_rows = 0, total_chunks = 0, num_m_tiles = 0, num_mc_tiles = 0, num_n_tiles = 0, num_k_blocks = 0;
   int group_m = 1, num_tiles = 0, stages = 0, mma_n = 0, tmem_cols = 0, splits = 1;
   uint32_t b_slot_bytes = 0;
   size_t smem_bytes = 0;
   dim3 grid{1, 1, 1};
   int cluster_x = 1;
   int full_tiles = 0, tail_tiles = 0, tail_splits = 1, num_items = 0;
+  int max_clusters = 0;  // co-resident clusters (rows path)
   size_t tail_bytes = 0;  // workspace bytes for tail counters and partials
   // descriptor cache: tensor maps depend only on the X and Y pointers
   bool cache_valid = false;
@@ -164,6 +165,7 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
   if (best_bh > 0 && force_path != kPathRows) {
     pl->key.path = kPathSwap;
     pl->key.bn = kTileM;
+    pl->key.cm = 1;
     pl->box_rows = best_bh;
     pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, best_bh));
     pl->mma_n = (int)((best_pad + 31) / 32 * 32);
@@ -206,9 +208,16 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, bh_best));
     pl->num_m_tiles = (int)tiles_best;
     pl->num_n_tiles = (int)(pl->n / bn);
-    if ((int64_t)pl->num_m_tiles * pl->num_n_tiles > ((int64_t)1 << 31) - 1)
+    // Clusters of two CTAs on neighbouring row tiles share each Y tile through
+    // TMA multicast (each loads half), cutting per-SM operand traffic by a third.
+    int cm = pl->num_m_tiles >= 2 ? 2 : 1;
+    const int env_cm = env_int("AGMM_CM", 0);
+    if (env_cm == 1 || env_cm == 2) cm = env_cm;
+    pl->key.cm = cm;
+    pl->num_mc_tiles = (pl->num_m_tiles + cm - 1) / cm;
+    if ((int64_t)pl->num_mc_tiles * pl->num_n_tiles > ((int64_t)1 << 31) - 1)
       return fail(AGMM_ERR_INVALID_ARG, "too many output tiles");
-    pl->num_tiles = pl->num_m_tiles * pl->num_n_tiles;
+    pl->num_tiles = pl->num_mc_tiles * pl->num_n_tiles;
     pl->mma_n = bn;
     pl->b_slot_bytes = (uint32_t)bn * 128u;
     const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
@@ -281,10 +290,19 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       pl->smem_bytes = 1024 + (size_t)pl->stages * stage_bytes + kCtlBytes;
     }
     int active = 0;
-    e = prepare_agmm_kernel(pl->key, pl->smem_bytes, pl->splits, &active);
+    const int cluster = pl->key.path == kPathSwap ? pl->splits : pl->key.cm;
+    e = prepare_agmm_kernel(pl->key, pl->smem_bytes, cluster, &active);
     if (e != cudaSuccess) {
       delete pl;
       return fail_cuda(e, "kernel attribute setup");
+    }
+    if (pl->key.path == kPathRows) {
+      if (active <= 0) {
+        delete pl;
+        return fail(AGMM_ERR_UNSUPPORTED, "row kernel cannot be resident");
+      }
+      pl->max_clusters = cluster > 1 ? active : active * pl->num_sms;
+      break;
     }
     if (pl->splits == 1) active *= pl->num_sms;  // CTAs per SM -> CTAs per device
     const int needed = pl->key.path == kPathSwap ? pl->num_n_tiles : 1;
@@ -299,9 +317,11 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
     pl->grid = dim3((unsigned)pl->splits, (unsigned)pl->num_n_tiles, 1);
     pl->cluster_x = pl->splits;
   } else {
-    // Persistent CTAs, one per SM.  The last, partial wave of tiles is split
-    // along k so that it keeps every SM busy: each tail tile becomes s parts.
-    const int G = pl->num_sms;
+    // Persistent clusters, one CTA per SM.  The last, partial wave of cluster
+    // tiles is split along k so that it keeps every SM busy: each tail tile
+    // becomes s parts.
+    const int cm = pl->key.cm;
+    const int G = std::max(1, std::min(pl->num_sms / cm, pl->max_clusters));
     const int W = pl->num_tiles / G;
     const int R = pl->num_tiles - W * G;
     int s_tail = 1;
@@ -313,17 +333,17 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       pl->full_tiles = W * G;
       pl->tail_tiles = R;
       pl->num_items = pl->full_tiles + R * s_tail;
-      pl->grid = dim3((unsigned)(W > 0 ? G : R * s_tail), 1, 1);
-      pl->tail_bytes = (size_t)(R * 4 + 255) / 256 * 256 +
-                       (size_t)R * (s_tail - 1) * kTileM * (size_t)pl->key.bn * 4;
+      pl->grid = dim3((unsigned)((W > 0 ? G : R * s_tail) * cm), 1, 1);
+      pl->tail_bytes = (size_t)(R * cm * 4 + 255) / 256 * 256 +
+                       (size_t)R * cm * (s_tail - 1) * kTileM * (size_t)pl->key.bn * 4;
     } else {
       pl->full_tiles = pl->num_tiles;
       pl->tail_tiles = 0;
       pl->num_items = pl->num_tiles;
-      pl->grid = dim3((unsigned)std::min(pl->num_tiles, G), 1, 1);
+      pl->grid = dim3((unsigned)(std::min(pl->num_tiles, G) * cm), 1, 1);
       pl->tail_bytes = 0;
     }
-    pl->cluster_x = 1;
+    pl->cluster_x = cm;
   }
   KernelParams& kp = pl->params;
   kp.m_pd = m_pd;
@@ -334,6 +354,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   while ((1 << kp.box_shift) < pl->box_rows) ++kp.box_shift;
   kp.total_chunks = pl->total_chunks;
   kp.num_m_tiles = pl->num_m_tiles;
+  kp.num_mc_tiles = pl->num_mc_tiles;
   kp.num_n_tiles = pl->num_n_tiles;
   kp.num_k_blocks = pl->num_k_blocks;
   kp.group_m = pl->group_m;
@@ -394,7 +415,8 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
       }
     }
     bool ok;
-    const uint32_t y_rows = pl->key.path == kPathSwap ? (uint32_t)kTileM : (uint32_t)pl->key.bn;
+    const uint32_t y_rows =
+        pl->key.path == kPathSwap ? (uint32_t)kTileM : (uint32_t)(pl->key.bn / pl->key.cm);
     if (pl->rhs_t)  // Y [n, k]: K-major boxes of y_rows n-rows
       ok = encode_2d(&kp.ymap, y, (uint64_t)pl->k, (uint64_t)pl->n, kTileK, y_rows, &err);
     else  // Y [k, n]: MN-major boxes of 64 n x 64 k
@@ -412,15 +434,18 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
   kp.my_id = my_id;
   if (pl->tail_splits > 1) {
     kp.tail_flags = static_cast<int*>(tail_ws);
-    kp.tail_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(tail_ws) + (pl->tail_tiles * 4 + 255) / 256 * 256);
+    kp.tail_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(tail_ws) +
+                                                (pl->tail_tiles * pl->key.cm * 4 + 255) / 256 * 256);
   } else {
     kp.tail_flags = nullptr;
     kp.tail_partials = nullptr;
   }
-  // Tail owners wait for other CTAs: a cooperative launch guarantees that
-  // every CTA of the grid is resident at once.
+  // Tail owners wait for other CTAs.  Without clusters a cooperative launch
+  // guarantees that every CTA of the grid is resident at once; with clusters
+  // the planner sized the grid to the co-resident cluster count, and the
+  // owners' waits are bounded in any case.
   cudaError_t e = launch_agmm_kernel(pl->key, kp, pl->grid, pl->cluster_x, pl->smem_bytes,
-                                     pl->tail_splits > 1, stream);
+                                     pl->tail_splits > 1 && pl->cluster_x == 1, stream);
   if (e != cudaSuccess) return fail_cuda(e, "fused kernel launch");
   return AGMM_OK;
 }

@@ -59,18 +59,27 @@ static_assert(kChunkTabOffset + kMaxSwapChunks * 16 <= kCtlBytes, "control block
 
 enum WaitResult : int { kWaitOk = 1, kWaitTimeout = 0, kWaitAborted = -1 };
 
-// Bounded wait for the phase of `bar` with the given parity.
+// Bounded wait for the phase of `bar` with the given parity.  When `waited`
+// is given, the time spent blocked is added to it (trace only).
 __device__ __forceinline__ int wait_phase(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns) {
+                                          uint64_t limit_ns, uint64_t* waited = nullptr) {
   if (ptx::mbar_try_wait(bar, parity)) return kWaitOk;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return kWaitOk;
+    if (ptx::mbar_try_wait(bar, parity)) {
+      if (waited) *waited += ptx::globaltimer_ns() - t0;
+      return kWaitOk;
+    }
     if ((it & 15u) == 0u) {
       if (*abort) return kWaitAborted;
       if (ptx::globaltimer_ns() - t0 > limit_ns) return kWaitTimeout;
     }
   }
+}
+
+// Trace slot written by one thread (not lane 0 of each warp).
+__device__ __forceinline__ void trace_value(const KernelParams& p, int slot, uint64_t v) {
+  if (p.trace != nullptr) p.trace[(size_t)(blockIdx.x + gridDim.x * blockIdx.y) * kTraceSlots + slot] = v;
 }
 
 // Bounded wait that ignores the abort flag: used to drain work in flight.
@@ -113,7 +122,7 @@ __device__ __forceinline__ void decode_row_tile(const KernelParams& p, int tile,
   const int per_group = p.group_m * p.num_n_tiles;
   const int grp = tile / per_group;
   const int first_m = grp * p.group_m;
-  const int gm = min(p.num_m_tiles - first_m, p.group_m);
+  const int gm = min(p.num_mc_tiles - first_m, p.group_m);
   const int r = tile - grp * per_group;
   mt = first_m + r % gm;
   nt = r / gm;
@@ -127,7 +136,10 @@ struct WorkItem {
   int tail;      // index of the tail tile, -1 for a whole tile
 };
 
-__device__ __forceinline__ WorkItem decode_rows_item(const KernelParams& p, int item) {
+// Work item `item` of a cluster: a cluster tile (cluster row mc, n tile nt),
+// whole or one k part of a split tail tile.  CTA `crank` of the cluster takes
+// row tile mc * cm + crank.
+__device__ __forceinline__ WorkItem decode_rows_item(const KernelParams& p, int item, int cm, int crank) {
   WorkItem w;
   int tile;
   if (item < p.full_tiles) {
@@ -147,6 +159,7 @@ __device__ __forceinline__ WorkItem decode_rows_item(const KernelParams& p, int 
     w.kb1 = (int)((int64_t)(w.part + 1) * p.num_k_blocks / w.nparts);
   }
   decode_row_tile(p, tile, w.mt, w.nt);
+  w.mt = w.mt * cm + crank;
   return w;
 }
 
@@ -212,8 +225,9 @@ __device__ __forceinline__ void store_row4(void* out, int64_t ldo, int64_t row, 
 // (K-major tiles); otherwise Y is [k, n] and its tiles are MN-major.  kF32:
 // float32 output.  kBN: n tile of the rows path (the swap path uses 128).
 // ----------------------------------------------------------------------------
-template <int kPath, bool kYK, bool kF32, int kBN>
+template <int kPath, bool kYK, bool kF32, int kBN, int kCM>
 __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_constant__ KernelParams p) {
+  static_assert(kCM == 1 || (kPath == kPathRows && (kYK || kBN / 64 >= kCM)), "bad cluster multicast shape");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -236,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar_full(ctl, s), 1);
-      ptx::mbar_init(bar_empty(ctl, s), 1);
+      ptx::mbar_init(bar_empty(ctl, s), kCM);  // every cluster CTA's MMA frees the stage
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_acc_full(ctl, a), 1);
@@ -282,8 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   const int kb_begin = (kPath == kPathSwap) ? (int)((int64_t)split * p.num_k_blocks / p.splits) : 0;
   const int kb_end =
       (kPath == kPathSwap) ? (int)((int64_t)(split + 1) * p.num_k_blocks / p.splits) : p.num_k_blocks;
-  const int tile_first = (kPath == kPathSwap) ? 0 : (int)blockIdx.x;
-  const int tile_step = (kPath == kPathSwap) ? 1 : (int)gridDim.x;
+  const int crank = (kCM > 1) ? (int)(blockIdx.x % kCM) : 0;  // rank in the cluster
+  const uint16_t cmask = (uint16_t)((1u << kCM) - 1u);
+  const int tile_first = (kPath == kPathSwap) ? 0 : (int)(blockIdx.x / kCM);
+  const int tile_step = (kPath == kPathSwap) ? 1 : (int)(gridDim.x / kCM);
   const int tile_count = (kPath == kPathSwap) ? 1 : p.num_items;
 
   if (warp == 0) {
@@ -295,6 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       bool dropped = false;
       bool ok = true;
       bool traced_first = false;
+      uint64_t waited_empty = 0;
+      uint64_t* wait_acc = p.trace ? &waited_empty : nullptr;
       const int cpt = kTileM / p.box_rows;
       for (int tile = tile_first; ok && tile < tile_count; tile += tile_step) {
         int mt = 0, nt = swap_nt;
@@ -304,14 +322,14 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         int nchunks = 0;
         uint32_t bytes;
         if constexpr (kPath == kPathRows) {
-          const WorkItem wi = decode_rows_item(p, tile);
+          const WorkItem wi = decode_rows_item(p, tile, kCM, crank);
           mt = wi.mt;
           nt = wi.nt;
           kb0 = wi.kb0;
           kb1 = wi.kb1;
           for (int j = 0; j < cpt; ++j) {
             const int64_t gc = (int64_t)mt * cpt + j;
-            if (gc < p.total_chunks) {
+            if (mt < p.num_m_tiles && gc < p.total_chunks) {
               const RingChunk ch = ring_chunk(geom, gc);
               shard_j[nchunks] = ch.shard;
               row_j[nchunks] = (int)ch.src_row;
@@ -323,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           bytes = (uint32_t)kASlotBytes + (uint32_t)p.total_chunks * p.box_rows * 128u;
         }
         for (int kb = kb0; kb < kb1; ++kb) {
-          const int res = wait_phase(bar_empty(ctl, stage), phase ^ 1u, abort_flag, limit);
+          const int res = wait_phase(bar_empty(ctl, stage), phase ^ 1u, abort_flag, limit, wait_acc);
           if (res != kWaitOk) {
             record_failure(p, abort_flag, res, kRoleProducer, stage, tile);
             ok = false;
@@ -343,12 +361,29 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
               for (int j = 0; j < nchunks; ++j)
                 ptx::tma_load_2d(a_dst + (uint32_t)j * p.box_rows * 128u, &p.xmap[shard_j[j]], full,
                                  k0, row_j[j]);
-              if constexpr (kYK) {
-                ptx::tma_load_2d(b_dst, &p.ymap, full, k0, nt * kBN);
-              } else {
+              if constexpr (kCM == 1) {
+                if constexpr (kYK) {
+                  ptx::tma_load_2d(b_dst, &p.ymap, full, k0, nt * kBN);
+                } else {
 #pragma unroll
-                for (int a = 0; a < kBN / 64; ++a)
-                  ptx::tma_load_2d(b_dst + (uint32_t)a * 8192u, &p.ymap, full, nt * kBN + a * 64, k0);
+                  for (int a = 0; a < kBN / 64; ++a)
+                    ptx::tma_load_2d(b_dst + (uint32_t)a * 8192u, &p.ymap, full, nt * kBN + a * 64, k0);
+                }
+              } else {
+                // This CTA's share of the Y tile, multicast to the whole cluster.
+                if constexpr (kYK) {
+                  constexpr int kRows = kBN / kCM;
+                  ptx::tma_load_2d_multicast(b_dst + (uint32_t)(crank * kRows) * 128u, &p.ymap, full, k0,
+                                             nt * kBN + crank * kRows, cmask);
+                } else {
+                  constexpr int kBoxes = kBN / 64 / kCM;
+#pragma unroll
+                  for (int aa = 0; aa < kBoxes; ++aa) {
+                    const int a = crank * kBoxes + aa;
+                    ptx::tma_load_2d_multicast(b_dst + (uint32_t)a * 8192u, &p.ymap, full, nt * kBN + a * 64, k0,
+                                               cmask);
+                  }
+                }
               }
             } else {
               if constexpr (kYK) {
@@ -376,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         }
       }
       trace(p, 3);
+      if (kPath == kPathRows) trace_value(p, 10, waited_empty);
       // Wait for this thread's TMA loads still in flight (only on an abort can
       // a load be unconsumed; a consumed stage's phase has already completed).
       for (int s = 0; s < S; ++s)
@@ -396,10 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
+      uint64_t waited_full = 0, waited_accfree = 0;
+      uint64_t* wf = p.trace ? &waited_full : nullptr;
+      uint64_t* wa = p.trace ? &waited_accfree : nullptr;
       for (int tile = tile_first; ok && tile < tile_count; tile += tile_step, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-        int res = wait_phase(bar_acc_empty(ctl, acc), acc_phase ^ 1u, abort_flag, limit);
+        int res = wait_phase(bar_acc_empty(ctl, acc), acc_phase ^ 1u, abort_flag, limit, wa);
         if (res != kWaitOk) {
           record_failure(p, abort_flag, res, kRoleMma, -1, tile);
           break;
@@ -408,12 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * mma_n);
         int kb0 = kb_begin, kb1 = kb_end;
         if constexpr (kPath == kPathRows) {
-          const WorkItem wi = decode_rows_item(p, tile);
+          const WorkItem wi = decode_rows_item(p, tile, kCM, crank);
           kb0 = wi.kb0;
           kb1 = wi.kb1;
         }
         for (int kb = kb0; kb < kb1; ++kb) {
-          res = wait_phase(bar_full(ctl, stage), phase, abort_flag, limit);
+          res = wait_phase(bar_full(ctl, stage), phase, abort_flag, limit, wf);
           if (res != kWaitOk) {
             record_failure(p, abort_flag, res, kRoleMma, stage, tile);
             ok = false;
@@ -435,7 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
                      : ptx::smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
             ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(bar_empty(ctl, stage));  // frees the stage once these MMAs finish
+          // frees the stage (in every cluster CTA: their producers multicast
+          // into it) once these MMAs finish
+          if constexpr (kCM > 1)
+            ptx::mma_commit_multicast(bar_empty(ctl, stage), cmask);
+          else
+            ptx::mma_commit(bar_empty(ctl, stage));
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -445,6 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         ptx::mma_commit(bar_acc_full(ctl, acc));  // accumulator ready for the epilogue
       }
       trace(p, 5);
+      trace_value(p, 14, waited_full);
+      trace_value(p, 15, waited_accfree);
       // Every MMA this thread issued has finished once the drain barrier fires.
       ptx::mma_commit(bar_drain(ctl));
       if (!wait_drain(bar_drain(ctl), 0, limit))
@@ -458,11 +504,13 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     if constexpr (kPath == kPathRows) {
       const int cpt = kTileM / p.box_rows;
       int it = 0;
+      uint64_t waited_accfull = 0;
+      uint64_t* we = p.trace ? &waited_accfull : nullptr;
       for (int tile = tile_first; tile < tile_count; tile += tile_step, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         int res = kWaitOk;
-        if (lane == 0) res = wait_phase(bar_acc_full(ctl, acc), acc_phase, abort_flag, limit);
+        if (lane == 0) res = wait_phase(bar_acc_full(ctl, acc), acc_phase, abort_flag, limit, we);
         res = __shfl_sync(0xffffffffu, res, 0);
         if (res != kWaitOk) {
           if (lane == 0) record_failure(p, abort_flag, res, kRoleEpilogue, acc, tile);
@@ -470,25 +518,26 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         }
         ptx::tc_fence_after();
         if (it == 0) trace(p, 6);
-        const WorkItem wi = decode_rows_item(p, tile);
+        const WorkItem wi = decode_rows_item(p, tile, kCM, crank);
         const int64_t gc = (int64_t)wi.mt * cpt + trow / p.box_rows;
         const int r = trow % p.box_rows;
         int64_t out_row = -1;
-        if (gc < p.total_chunks) {
+        if (wi.mt < p.num_m_tiles && gc < p.total_chunks) {
           const RingChunk ch = ring_chunk(geom, gc);
           if (r < ch.valid) out_row = ch.out_row + r;
         }
         const uint32_t tbase = lane_base + (uint32_t)(acc * kBN);
         // Partial slots of this tail tile: [part-1][BN/32][128 rows][32 floats].
         const size_t slot_floats = (size_t)kTileM * kBN;
+        const int tail_slot = wi.tail * kCM + crank;
         float* tail_base = (wi.tail >= 0)
-                               ? p.tail_partials + (size_t)wi.tail * (wi.nparts - 1) * slot_floats
+                               ? p.tail_partials + (size_t)tail_slot * (wi.nparts - 1) * slot_floats
                                : nullptr;
         if (wi.nparts > 1 && wi.part == 0) {
           // Owner: wait (bounded) until the other parts have published.
           int wres = kWaitOk;
           if (threadIdx.x == 64) {
-            const int* flag = p.tail_flags + wi.tail;
+            const int* flag = p.tail_flags + tail_slot;
             const uint64_t t0 = ptx::globaltimer_ns();
             while (ld_acquire_gpu(flag) < wi.nparts - 1) {
               if (*abort_flag) { wres = kWaitAborted; break; }
@@ -538,10 +587,11 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           // Publish: every thread's stores, then one arrival for the tile.
           __threadfence();
           epilogue_bar_sync();
-          if (threadIdx.x == 64) atomicAdd(p.tail_flags + wi.tail, 1);
+          if (threadIdx.x == 64) atomicAdd(p.tail_flags + tail_slot, 1);
         }
       }
       trace(p, 7);
+      if (warp == 2 && lane == 0) trace_value(p, 9, waited_accfull);
     } else {
       // Swap path: wait for this CTA's float32 partial [n 128][row slots].
       int res = kWaitOk;
@@ -660,6 +710,12 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     trace(p, 10);
   }
 
+  if constexpr (kPath == kPathRows && kCM > 1) {
+    // Peers multicast into this CTA's shared memory and arrive on its
+    // barriers until their last MMA commits: leave only after all have drained.
+    __syncwarp();
+    ptx::cluster_sync_all();
+  }
   __syncthreads();
   if (warp == 0) trace(p, 11);
   if (warp == 1) {
@@ -694,14 +750,19 @@ __global__ void __launch_bounds__(256) agmm_gather_rows(const __grid_constant__ 
 using KernelFn = void (*)(KernelParams);
 
 KernelFn select_kernel(const KernelKey& k) {
-#define AGMM_PICK(PATH, BN)                                                                   \
-  (k.y_kmajor ? (k.out_f32 ? &agmm_fused_sm103a<PATH, true, true, BN>                         \
-                           : &agmm_fused_sm103a<PATH, true, false, BN>)                       \
-              : (k.out_f32 ? &agmm_fused_sm103a<PATH, false, true, BN>                        \
-                           : &agmm_fused_sm103a<PATH, false, false, BN>))
-  if (k.path == kPathSwap) return AGMM_PICK(kPathSwap, 128);
-  if (k.bn == 256) return AGMM_PICK(kPathRows, 256);
-  if (k.bn == 128) return AGMM_PICK(kPathRows, 128);
+#define AGMM_PICK(PATH, BN, CM)                                                              \
+  (k.y_kmajor ? (k.out_f32 ? &agmm_fused_sm103a<PATH, true, true, BN, CM>                    \
+                           : &agmm_fused_sm103a<PATH, true, false, BN, CM>)                  \
+              : (k.out_f32 ? &agmm_fused_sm103a<PATH, false, true, BN, CM>                   \
+                           : &agmm_fused_sm103a<PATH, false, false, BN, CM>))
+  if (k.path == kPathSwap) return k.cm == 1 ? AGMM_PICK(kPathSwap, 128, 1) : nullptr;
+  if (k.cm == 1) {
+    if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 1);
+    if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 1);
+  } else if (k.cm == 2) {
+    if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2);
+    if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2);
+  }
   return nullptr;
 #undef AGMM_PICK
 }

@@ -39,10 +39,11 @@ struct __align__(64) KernelParams {
   int box_shift;                 // log2(box_rows)
   int total_chunks;              // chunks in the ring-ordered row sequence
   int num_m_tiles;               // row path: 128-row tiles of chunks
+  int num_mc_tiles;              // row path: cluster rows = ceil(num_m_tiles / CTAs per cluster)
   int num_n_tiles;               // n tiles
   int num_k_blocks;              // k / 64
   int group_m;                   // row path: row tiles per raster group
-  int num_tiles;                 // row path: num_m_tiles * num_n_tiles
+  int num_tiles;                 // row path: num_mc_tiles * num_n_tiles (cluster tiles)
   int stages;                    // pipeline depth (<= kMaxStages)
   int mma_n;                     // MMA N
   int tmem_cols;                 // TMEM columns allocated (power of two >= 32)
@@ -60,8 +61,8 @@ struct __align__(64) KernelParams {
   int full_tiles;
   int tail_splits;
   int num_items;
-  int* tail_flags;               // [tail tiles] arrival counters (zero between runs)
-  float* tail_partials;          // [tail tiles][tail_splits-1][BN/32][128][32]
+  int* tail_flags;               // [tail tiles][cluster rank] arrival counters (zero between runs)
+  float* tail_partials;          // [tail tiles][cluster rank][tail_splits-1][BN/32][128][32]
 };
 
 struct GatherParams {
@@ -77,6 +78,7 @@ struct KernelKey {
   bool y_kmajor;
   bool out_f32;
   int bn;
+  int cm;  // row path: CTAs per cluster along M sharing each Y tile by TMA multicast
 };
 
 // Largest dynamic shared memory a CTA may request (227 KiB on sm_100-class parts).

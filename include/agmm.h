@@ -167,8 +167,12 @@ agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream)
  * (2, 3), first operand arrival at the MMA thread (4), last MMA commit (5),
  * first accumulator seen by the epilogue (6), rows-path epilogue done (7),
  * swap-path reduction barriers (8, 9), reduction stored (10), exit (11), plus
- * the SM id (12) and cluster rank (13).  Pass NULL to switch it off.  The
- * buffer stays owned by the caller and must outlive the runs that use it.
+ * the SM id (12) and cluster rank (13).  On the row path slots 9, 10, 14 and
+ * 15 instead hold nanoseconds spent blocked: epilogue waiting for an
+ * accumulator (9), producer waiting for a free stage (10), MMA thread waiting
+ * for operands (14) and for a free accumulator (15).  Pass NULL to switch it
+ * off.  The buffer stays owned by the caller and must outlive the runs that
+ * use it.
  */
 size_t agmm_trace_bytes(agmm_plan_t plan);
 agmm_status_t agmm_set_trace(agmm_plan_t plan, void* trace, size_t bytes);

@@ -144,3 +144,21 @@ def test_tail_split_parts(agmm, tail, monkeypatch):
         # a second run reuses the zeroed counters
         o2, _ = _run(agmm, xs_cpu, y_cpu, rt, my_id=1, plan=plan)
         assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+
+
+@pytest.mark.parametrize("case", [(3, 200, 1024, 512, False), (5, 300, 512, 256, True), (8, 130, 256, 640, True)])
+def test_cluster_multicast_matches_single_cta(agmm, case, monkeypatch):
+    # Pairs of CTAs share each Y tile through TMA multicast; with no tail split
+    # the arithmetic is unchanged, so the output is bitwise equal to one CTA
+    # per cluster.  Odd row-tile counts exercise the idle second CTA.
+    P, m, k, n, rt = case
+    xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=6)
+    ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+    monkeypatch.setenv("AGMM_TAIL_SPLIT", "1")
+    outs = {}
+    for cm in ("1", "2"):
+        monkeypatch.setenv("AGMM_CM", cm)
+        o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=P - 1)
+        check(o, ref32, f"cm={cm} {plan.info()}")
+        outs[cm] = o
+    assert torch.equal(outs["1"].view(torch.int16), outs["2"].view(torch.int16))
