@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = [
     "agmm_plan", "agmm_destroy", "agmm_workspace_bytes", "agmm_run", "agmm_run_unfused",
     "agmm_run_host", "agmm_query_status", "agmm_plan_info", "agmm_ring_chunks",
     "agmm_status_string", "agmm_last_error", "agmm_version", "agmm_trace_bytes", "agmm_set_trace",
+    "agmm_run_unfused_noalloc",
 ]
 
 
@@ -89,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.agmm_last_error.restype = ctypes.c_char_p
     lib.agmm_version.argtypes = []
     lib.agmm_version.restype = c_int
+    lib.agmm_run_unfused_noalloc.argtypes = [vp, ctypes.POINTER(vp), vp, vp, c_int, vp]
+    lib.agmm_run_unfused_noalloc.restype = c_int
     lib.agmm_trace_bytes.argtypes = [vp]
     lib.agmm_trace_bytes.restype = ctypes.c_size_t
     lib.agmm_set_trace.argtypes = [vp, vp, ctypes.c_size_t]

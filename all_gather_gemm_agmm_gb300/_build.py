@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libagmm.so")
-SOURCES = ["agmm_kernels.cu", "agmm_api.cpp"]
+SOURCES = ["agmm_kernels.cu", "agmm_api.cpp", "agmm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

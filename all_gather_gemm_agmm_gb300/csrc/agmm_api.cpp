@@ -127,6 +127,8 @@ struct agmm_plan_s {
 
 namespace {
 
+size_t gathered_bytes(const agmm_plan_s* pl) { return ((size_t)pl->M() * (size_t)pl->k * 2 + 255) / 256 * 256; }
+
 agmm_status_t validate_shape(int P, int64_t m_pd, int64_t k, int64_t n, int dtype, int rhs_t) {
   if (P < 1 || P > AGMM_MAX_SHARDS)
     return fail(AGMM_ERR_INVALID_ARG, "P must be in [1, 8] (per-peer descriptor tables hold at most 8)");
@@ -452,6 +454,50 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
 
 }  // namespace
 
+namespace agmm {
+
+// Records a failure for agmm_last_error (used by other translation units).
+agmm_status_t set_last_error(agmm_status_t status, const char* message) { return fail(status, message); }
+
+// The unfused path on an explicit scratch region of scratch_bytes bytes, with
+// the status words and split-tail counters cleared first on `stream`.  Used by
+// the allocation-free entry point.
+agmm_status_t run_unfused_on_scratch(agmm_plan_s* plan, const void* const* x_shards, const void* y, void* o,
+                                     int my_id, void* scratch, size_t scratch_bytes, cudaStream_t s) {
+  if (!plan) return fail(AGMM_ERR_INVALID_ARG, "plan is NULL");
+  const size_t need = agmm_workspace_bytes(plan, 1);
+  if (need > scratch_bytes)
+    return fail(AGMM_ERR_INVALID_ARG, "this problem needs " + std::to_string(need) +
+                                          " bytes of scratch but the static scratch holds " +
+                                          std::to_string(scratch_bytes) + "; use agmm_run_unfused");
+  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, scratch);
+  if (st != AGMM_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  agmm_plan_s* gemm = plan->P == 1 ? plan : plan->sub;
+  uint8_t* tail = plan->P == 1 ? base + kStatusBytes : base + kStatusBytes + gathered_bytes(plan);
+  cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes, s);
+  if (e == cudaSuccess && gemm->tail_splits > 1)
+    e = cudaMemsetAsync(tail, 0, (size_t)(gemm->tail_tiles * gemm->key.cm * 4 + 255) / 256 * 256, s);
+  if (e != cudaSuccess) return fail_cuda(e, "scratch clear");
+  if (plan->P == 1) return launch_fused(plan, x_shards, y, o, 0, base, tail, s);
+  uint8_t* gathered = base + kStatusBytes;
+  for (int r = 0; r < plan->P; ++r)
+    if (overlaps(x_shards[r], (size_t)plan->m_pd * plan->k * 2, gathered, gathered_bytes(plan)))
+      return fail(AGMM_ERR_INVALID_ARG, "the scratch overlaps a shard");
+  GatherParams g{};
+  for (int r = 0; r < plan->P; ++r) g.src[r] = static_cast<const uint4*>(x_shards[r]);
+  g.dst = reinterpret_cast<uint4*>(gathered);
+  g.vec_per_shard = plan->m_pd * plan->k * 2 / 16;
+  const int64_t want = (g.vec_per_shard + 4 * 256 - 1) / (4 * 256);
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)plan->num_sms * 8 / plan->P + 1));
+  e = launch_gather_kernel(g, plan->P, blocks, s);
+  if (e != cudaSuccess) return fail_cuda(e, "gather kernel launch");
+  const void* one[1] = {gathered};
+  return launch_fused(plan->sub, one, y, o, 0, base, tail, s);
+}
+
+}  // namespace agmm
+
 extern "C" {
 
 agmm_status_t agmm_plan(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
@@ -469,10 +515,6 @@ void agmm_destroy(agmm_plan_t plan) {
   agmm_destroy(plan->sub);
   delete plan;
 }
-
-namespace {
-size_t gathered_bytes(const agmm_plan_s* pl) { return ((size_t)pl->M() * (size_t)pl->k * 2 + 255) / 256 * 256; }
-}  // namespace
 
 size_t agmm_workspace_bytes(agmm_plan_t plan, int unfused) {
   if (!plan) return 0;

@@ -143,6 +143,30 @@ agmm_status_t agmm_run_unfused(agmm_plan_t plan, const void* const* x_shards, co
                                void* o, int my_id, void* workspace, void* stream);
 
 /*
+ * agmm_run_unfused_noalloc -- agmm_run_unfused without a caller workspace and
+ * without allocating: for callers that cannot allocate device memory where
+ * they run this (inside CUDA graph capture, under an allocator that owns all
+ * device memory, or in latency-critical loops that cannot afford cudaMalloc's
+ * implicit synchronisation).  The pages have no counterpart; this is a
+ * convenience of this library.
+ *
+ * The scratch is one file-scope device array of AGMM_STATIC_SCRATCH_BYTES that
+ * every GPU loading this library holds until the process exits.  A problem
+ * whose agmm_workspace_bytes(plan, 1) exceeds it is rejected with
+ * AGMM_ERR_INVALID_ARG (nothing is launched).  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  Each call clears the scratch's status words and
+ * counters on `stream`, then gathers and multiplies.  All calls share the one
+ * array: calls that overlap on the device (different streams without ordering)
+ * race and corrupt each other.  Device-side wait timeouts of these calls are
+ * recorded in the shared scratch and are not reported to the caller.
+ * Arguments, alignment rules and result are those of agmm_run.
+ */
+#define AGMM_STATIC_SCRATCH_BYTES ((size_t)64 << 20) /* 64 MiB */
+agmm_status_t agmm_run_unfused_noalloc(agmm_plan_t plan, const void* const* x_shards, const void* y,
+                                       void* o, int my_id, void* stream);
+
+/*
  * agmm_run_host -- agmm_run from host memory: copies each host shard to
  * x_dev[r] and the host Y to y_dev, runs, and copies O back to o_host, all
  * asynchronously on `stream` (host buffers should be pinned for overlap; the
