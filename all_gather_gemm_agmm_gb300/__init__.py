@@ -44,7 +44,7 @@ class AgmmError(RuntimeError):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [
-        ("path", ctypes.c_int), ("box_rows", ctypes.c_int), ("chunks", ctypes.c_int),
+        ("path", ctypes.c_int), ("box_rows", ctypes.c_int), ("whole_shards", ctypes.c_int), ("chunks", ctypes.c_int),
         ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int),
         ("stages", ctypes.c_int), ("splits", ctypes.c_int), ("num_tiles", ctypes.c_int),
         ("num_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("num_sms", ctypes.c_int),
@@ -80,7 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.agmm_query_status.restype = c_int
     lib.agmm_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
     lib.agmm_plan_info.restype = c_int
-    lib.agmm_ring_chunks.argtypes = [c_int, i64, c_int, c_int, ctypes.POINTER(ctypes.c_int32),
+    lib.agmm_ring_chunks.argtypes = [c_int, i64, c_int, c_int, c_int, ctypes.POINTER(ctypes.c_int32),
                                      ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_int32),
                                      i64, ctypes.POINTER(i64)]
     lib.agmm_ring_chunks.restype = c_int
@@ -126,17 +126,19 @@ def _stream_handle(stream) -> Optional[int]:
     return int(stream)
 
 
-def ring_chunks(P: int, m_per_device: int, my_id: int, box_rows: int) -> Dict[str, List[int]]:
+def ring_chunks(P: int, m_per_device: int, my_id: int, box_rows: int, whole_shards: bool = False
+                ) -> Dict[str, List[int]]:
     """The ring-ordered row chunks (host logic of agmm_ring_chunks)."""
     lib = load_library()
     n = ctypes.c_int64(0)
-    _check(lib.agmm_ring_chunks(P, m_per_device, my_id, box_rows, None, None, None, None, 0, ctypes.byref(n)))
+    w = int(bool(whole_shards))
+    _check(lib.agmm_ring_chunks(P, m_per_device, my_id, box_rows, w, None, None, None, None, 0, ctypes.byref(n)))
     cnt = n.value
     shard = (ctypes.c_int32 * cnt)()
     src = (ctypes.c_int64 * cnt)()
     out = (ctypes.c_int64 * cnt)()
     valid = (ctypes.c_int32 * cnt)()
-    _check(lib.agmm_ring_chunks(P, m_per_device, my_id, box_rows, shard, src, out, valid, cnt, ctypes.byref(n)))
+    _check(lib.agmm_ring_chunks(P, m_per_device, my_id, box_rows, w, shard, src, out, valid, cnt, ctypes.byref(n)))
     return {"shard": list(shard), "src_row": list(src), "out_row": list(out), "valid": list(valid)}
 
 
@@ -193,6 +195,9 @@ class Plan:
         return int(self._lib.agmm_workspace_bytes(self._h, int(bool(unfused))))
 
     def new_workspace(self, unfused: bool = False, device=None):
+        """A zero-filled workspace.  It is zeroed on the current stream: launches
+        on another stream must first wait for it (the kernels rely on its
+        counters starting at zero)."""
         import torch
 
         return torch.zeros(self.workspace_bytes(unfused), dtype=torch.uint8, device=device or "cuda")

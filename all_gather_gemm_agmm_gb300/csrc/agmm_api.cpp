@@ -106,13 +106,14 @@ struct agmm_plan_s {
   int device = 0;
   int num_sms = 0;
   KernelKey key{};
+  int whole_shards = 0;
   int box_rows = 0, total_chunks = 0, num_m_tiles = 0, num_mc_tiles = 0, num_n_tiles = 0, num_k_blocks = 0;
   int group_m = 1, num_tiles = 0, stages = 0, mma_n = 0, tmem_cols = 0, splits = 1;
   uint32_t b_slot_bytes = 0;
   size_t smem_bytes = 0;
   dim3 grid{1, 1, 1};
   int cluster_x = 1;
-  int full_tiles = 0, tail_tiles = 0, tail_splits = 1, num_items = 0;
+  int dp_tiles = 0, sk_tiles = 0;
   int max_clusters = 0;  // co-resident clusters (rows path)
   size_t tail_bytes = 0;  // workspace bytes for tail counters and partials
   // descriptor cache: tensor maps depend only on the X and Y pointers
@@ -149,17 +150,28 @@ agmm_status_t validate_shape(int P, int64_t m_pd, int64_t k, int64_t n, int dtyp
 // Tile planning for a device with `num_sms` SMs (pure host logic).
 agmm_status_t choose_tiles(agmm_plan_s* pl) {
   const int force_path = env_int("AGMM_PATH", -1);
+  // AGMM_CHUNKS=half|whole restricts the chunking mode (tests, tuning).
+  const char* force_chunks = std::getenv("AGMM_CHUNKS");
+  const int whole_lo = (force_chunks && std::strcmp(force_chunks, "whole") == 0) ? 1 : 0;
+  const int whole_hi = (force_chunks && std::strcmp(force_chunks, "half") == 0) ? 0 : 1;
   // Swap path: the whole ring-ordered row sequence (chunks padded to their box
-  // height) fits in one MMA N of at most 256.  Pick the box height with the
-  // least padding, the largest on ties (fewer TMA boxes).
-  int best_bh = -1;
-  int64_t best_pad = 0;
-  for (int bh = 128; bh >= 8; bh >>= 1) {
-    const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh);
-    const int64_t pad = ring_padded_rows(g);
-    if (pad <= 256 && (best_bh < 0 || pad < best_pad)) {
-      best_bh = bh;
-      best_pad = pad;
+  // height) fits in one MMA N of at most 256.  Candidates: half-shard chunks
+  // (the ring's half split) or whole-shard chunks, each with box heights 8..128.
+  // Cost: padded rows (MMA N, reduction volume) plus 16 rows per chunk (one
+  // TMA box per chunk and stage).  Ties keep the half split and larger boxes.
+  int best_bh = -1, best_whole = 0;
+  int64_t best_pad = 0, best_cost = 0;
+  for (int whole = whole_lo; whole <= whole_hi; ++whole) {
+    for (int bh = 128; bh >= 8; bh >>= 1) {
+      const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh, whole);
+      const int64_t pad = ring_padded_rows(g);
+      const int64_t cost = pad + 16 * ring_total_chunks(g);
+      if (pad <= 256 && (best_bh < 0 || cost < best_cost)) {
+        best_bh = bh;
+        best_whole = whole;
+        best_pad = pad;
+        best_cost = cost;
+      }
     }
   }
   const int64_t budget = (int64_t)kMaxDynSmem - 1024 - kCtlBytes;
@@ -169,7 +181,8 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->key.bn = kTileM;
     pl->key.cm = 1;
     pl->box_rows = best_bh;
-    pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, best_bh));
+    pl->whole_shards = best_whole;
+    pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, best_bh, best_whole));
     pl->mma_n = (int)((best_pad + 31) / 32 * 32);
     pl->num_n_tiles = (int)(pl->n / kTileM);
     pl->num_m_tiles = 1;
@@ -189,25 +202,37 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->group_m = 1;
   } else {
     pl->key.path = kPathRows;
-    // Box height: fewest 128-row tiles, the largest box on ties.
-    int bh_best = 128;
-    int64_t tiles_best = -1;
-    for (int bh = 128; bh >= 8; bh >>= 1) {
-      const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh);
-      const int64_t cpt = kTileM / bh;
-      const int64_t t = (ring_total_chunks(g) + cpt - 1) / cpt;
-      if (tiles_best < 0 || t < tiles_best) {
-        tiles_best = t;
-        bh_best = bh;
+    // Chunking: half-shard (the ring's half split) or whole-shard chunks, box
+    // heights 8..128.  Within 3% of the fewest 128-row tiles, take the largest
+    // box (fewest TMA boxes per stage); ties keep the half split.
+    int64_t min_tiles = -1;
+    for (int whole = whole_lo; whole <= whole_hi; ++whole)
+      for (int bh = 128; bh >= 8; bh >>= 1) {
+        const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh, whole);
+        const int64_t t = (ring_total_chunks(g) + kTileM / bh - 1) / (kTileM / bh);
+        if (min_tiles < 0 || t < min_tiles) min_tiles = t;
       }
-    }
+    int bh_best = -1, whole_best = 0;
+    int64_t tiles_best = -1;
+    for (int whole = whole_lo; whole <= whole_hi; ++whole)
+      for (int bh = 128; bh >= 8; bh >>= 1) {
+        const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh, whole);
+        const int64_t t = (ring_total_chunks(g) + kTileM / bh - 1) / (kTileM / bh);
+        if (t * 100 > min_tiles * 103 && t > min_tiles) continue;
+        if (bh > bh_best) {
+          bh_best = bh;
+          whole_best = whole;
+          tiles_best = t;
+        }
+      }
     if (tiles_best > (int64_t)1 << 30) return fail(AGMM_ERR_INVALID_ARG, "too many row tiles");
     int bn = (pl->n % 256 == 0) ? 256 : 128;
     const int env_bn = env_int("AGMM_BN", 0);
     if ((env_bn == 128 || env_bn == 256) && pl->n % env_bn == 0) bn = env_bn;
     pl->key.bn = bn;
     pl->box_rows = bh_best;
-    pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, bh_best));
+    pl->whole_shards = whole_best;
+    pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, bh_best, whole_best));
     pl->num_m_tiles = (int)tiles_best;
     pl->num_n_tiles = (int)(pl->n / bn);
     // Clusters of two CTAs on neighbouring row tiles share each Y tile through
@@ -319,32 +344,28 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
     pl->grid = dim3((unsigned)pl->splits, (unsigned)pl->num_n_tiles, 1);
     pl->cluster_x = pl->splits;
   } else {
-    // Persistent clusters, one CTA per SM.  The last, partial wave of cluster
-    // tiles is split along k so that it keeps every SM busy: each tail tile
-    // becomes s parts.
+    // Persistent clusters, one CTA per SM.  Whole waves of cluster tiles are
+    // dealt round-robin; when the tile count is not a multiple of the
+    // clusters, the last one to two waves' k blocks are divided evenly over
+    // the clusters (stream-K), so no SM idles in a ragged last wave.
     const int cm = pl->key.cm;
-    const int G = std::max(1, std::min(pl->num_sms / cm, pl->max_clusters));
-    const int W = pl->num_tiles / G;
-    const int R = pl->num_tiles - W * G;
-    int s_tail = 1;
-    if (R > 0) s_tail = std::max(1, std::min({G / R, 8, pl->num_k_blocks / 4}));
-    const int env_tail = env_int("AGMM_TAIL_SPLIT", -1);
-    if (env_tail >= 0 && R > 0) s_tail = std::max(1, std::min({env_tail, G / R, pl->num_k_blocks}));
-    pl->tail_splits = s_tail;
-    if (s_tail > 1) {
-      pl->full_tiles = W * G;
-      pl->tail_tiles = R;
-      pl->num_items = pl->full_tiles + R * s_tail;
-      pl->grid = dim3((unsigned)((W > 0 ? G : R * s_tail) * cm), 1, 1);
-      pl->tail_bytes = (size_t)(R * cm * 4 + 255) / 256 * 256 +
-                       (size_t)R * cm * (s_tail - 1) * kTileM * (size_t)pl->key.bn * 4;
-    } else {
-      pl->full_tiles = pl->num_tiles;
-      pl->tail_tiles = 0;
-      pl->num_items = pl->num_tiles;
-      pl->grid = dim3((unsigned)(std::min(pl->num_tiles, G) * cm), 1, 1);
-      pl->tail_bytes = 0;
+    int G = std::max(1, std::min(pl->num_sms / cm, pl->max_clusters));
+    const int T = pl->num_tiles;
+    int dp = T;
+    if (T % G != 0 && env_int("AGMM_STREAMK", 1) != 0) {
+      const int W = T / G;
+      dp = W >= 1 ? (W - 1) * G : 0;
+      // at least 4 k blocks per cluster share
+      const int64_t units = (int64_t)(T - dp) * pl->num_k_blocks;
+      if (units < (int64_t)G * 4) G = (int)std::max<int64_t>(1, units / 4);
     }
+    if (dp == T) G = std::min(G, T);
+    pl->dp_tiles = dp;
+    pl->sk_tiles = T - dp;
+    pl->grid = dim3((unsigned)(G * cm), 1, 1);
+    pl->tail_bytes = pl->sk_tiles > 0 ? (size_t)(pl->sk_tiles * cm * 4 + 255) / 256 * 256 +
+                                            (size_t)G * cm * kTileM * (size_t)pl->key.bn * 4
+                                      : 0;
     pl->cluster_x = cm;
   }
   KernelParams& kp = pl->params;
@@ -352,6 +373,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.ldo = n;
   kp.P = P;
   kp.box_rows = pl->box_rows;
+  kp.whole_shards = pl->whole_shards;
   kp.box_shift = 0;
   while ((1 << kp.box_shift) < pl->box_rows) ++kp.box_shift;
   kp.total_chunks = pl->total_chunks;
@@ -368,9 +390,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.b_slot_bytes = pl->b_slot_bytes;
   kp.wait_limit_ns = (uint64_t)std::max(1, env_int("AGMM_WAIT_LIMIT_MS", 2000)) * 1000000ull;
   kp.test_drop_first_arrive = env_int("AGMM_TEST_DROP_ARRIVE", 0) != 0;
-  kp.full_tiles = pl->full_tiles;
-  kp.tail_splits = pl->tail_splits;
-  kp.num_items = pl->num_items;
+  kp.dp_tiles = pl->dp_tiles;
   if (with_sub && P > 1) {
     st = plan_impl(1, pl->M(), k, n, dtype, rhs_t, false, &pl->sub);
     if (st != AGMM_OK) {
@@ -434,20 +454,20 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
   kp.out = o;
   kp.status = static_cast<int*>(status);
   kp.my_id = my_id;
-  if (pl->tail_splits > 1) {
-    kp.tail_flags = static_cast<int*>(tail_ws);
-    kp.tail_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(tail_ws) +
-                                                (pl->tail_tiles * pl->key.cm * 4 + 255) / 256 * 256);
+  if (pl->sk_tiles > 0) {
+    kp.sk_flags = static_cast<int*>(tail_ws);
+    kp.sk_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(tail_ws) +
+                                              (pl->sk_tiles * pl->key.cm * 4 + 255) / 256 * 256);
   } else {
-    kp.tail_flags = nullptr;
-    kp.tail_partials = nullptr;
+    kp.sk_flags = nullptr;
+    kp.sk_partials = nullptr;
   }
-  // Tail owners wait for other CTAs.  Without clusters a cooperative launch
-  // guarantees that every CTA of the grid is resident at once; with clusters
-  // the planner sized the grid to the co-resident cluster count, and the
-  // owners' waits are bounded in any case.
+  // Stream-K owners wait for other CTAs.  Without clusters a cooperative
+  // launch guarantees that every CTA of the grid is resident at once; with
+  // clusters the planner sized the grid to the co-resident cluster count, and
+  // the owners' waits are bounded in any case.
   cudaError_t e = launch_agmm_kernel(pl->key, kp, pl->grid, pl->cluster_x, pl->smem_bytes,
-                                     pl->tail_splits > 1 && pl->cluster_x == 1, stream);
+                                     pl->sk_tiles > 0 && pl->cluster_x == 1, stream);
   if (e != cudaSuccess) return fail_cuda(e, "fused kernel launch");
   return AGMM_OK;
 }
@@ -476,8 +496,8 @@ agmm_status_t run_unfused_on_scratch(agmm_plan_s* plan, const void* const* x_sha
   agmm_plan_s* gemm = plan->P == 1 ? plan : plan->sub;
   uint8_t* tail = plan->P == 1 ? base + kStatusBytes : base + kStatusBytes + gathered_bytes(plan);
   cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes, s);
-  if (e == cudaSuccess && gemm->tail_splits > 1)
-    e = cudaMemsetAsync(tail, 0, (size_t)(gemm->tail_tiles * gemm->key.cm * 4 + 255) / 256 * 256, s);
+  if (e == cudaSuccess && gemm->sk_tiles > 0)
+    e = cudaMemsetAsync(tail, 0, (size_t)(gemm->sk_tiles * gemm->key.cm * 4 + 255) / 256 * 256, s);
   if (e != cudaSuccess) return fail_cuda(e, "scratch clear");
   if (plan->P == 1) return launch_fused(plan, x_shards, y, o, 0, base, tail, s);
   uint8_t* gathered = base + kStatusBytes;
@@ -586,7 +606,7 @@ agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail_cuda(e, "stream synchronize");
-  int words[4] = {0, 0, 0, 0};
+  int words[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if ((e = cudaMemcpy(words, workspace, sizeof words, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return fail_cuda(e, "status read");
   if (words[0] == 0) return AGMM_OK;
@@ -595,7 +615,8 @@ agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream)
   const char* role = (words[1] >= 1 && words[1] <= 4) ? roles[words[1]] : roles[0];
   return fail(words[0] == AGMM_ERR_TIMEOUT ? AGMM_ERR_TIMEOUT : AGMM_ERR_CUDA,
               std::string("device wait ran out in the ") + role + " role (stage " + std::to_string(words[2]) +
-                  ", tile " + std::to_string(words[3]) + ")");
+                  ", tile " + std::to_string(words[3]) + "; detail " + std::to_string(words[4]) + " " +
+                  std::to_string(words[5]) + " " + std::to_string(words[6]) + " " + std::to_string(words[7]) + ")");
 }
 
 size_t agmm_trace_bytes(agmm_plan_t plan) {
@@ -619,6 +640,7 @@ agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info) {
   if (!plan || !info) return fail(AGMM_ERR_INVALID_ARG, "NULL argument");
   info->path = plan->key.path;
   info->box_rows = plan->box_rows;
+  info->whole_shards = plan->whole_shards;
   info->chunks = plan->total_chunks;
   info->tile_m = kTileM;
   info->tile_n = plan->mma_n;
@@ -633,13 +655,14 @@ agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info) {
   return AGMM_OK;
 }
 
-agmm_status_t agmm_ring_chunks(int P, int64_t m_per_device, int my_id, int box_rows, int32_t* shard,
-                               int64_t* src_row, int64_t* out_row, int32_t* valid, int64_t max_chunks,
-                               int64_t* n_chunks) {
+agmm_status_t agmm_ring_chunks(int P, int64_t m_per_device, int my_id, int box_rows, int whole_shards,
+                               int32_t* shard, int64_t* src_row, int64_t* out_row, int32_t* valid,
+                               int64_t max_chunks, int64_t* n_chunks) {
   if (P < 1 || P > AGMM_MAX_SHARDS || m_per_device < 1 || my_id < 0 || my_id >= P || box_rows < 1 ||
       box_rows > 256 || !n_chunks || max_chunks < 0)
     return fail(AGMM_ERR_INVALID_ARG, "bad ring description arguments");
-  const RingGeom g = make_ring_geom(P, m_per_device, my_id, box_rows);
+  if (whole_shards != 0 && whole_shards != 1) return fail(AGMM_ERR_INVALID_ARG, "whole_shards must be 0 or 1");
+  const RingGeom g = make_ring_geom(P, m_per_device, my_id, box_rows, whole_shards);
   const int64_t total = ring_total_chunks(g);
   *n_chunks = total;
   for (int64_t c = 0; c < total && c < max_chunks; ++c) {

@@ -52,7 +52,11 @@ __device__ __forceinline__ uint32_t bar_acc_empty(uint32_t ctl, int a) {
 __device__ __forceinline__ uint32_t bar_drain(uint32_t ctl) {
   return ctl + 8u * (2 * kMaxStages + 4);
 }
-constexpr int kAbortOffset = 8 * (2 * kMaxStages + 5);  // int
+// Stream-K hand-offs among the epilogue warps: the owner thread's go-ahead
+// (1 arrival) and the contributors' "partial stored" (128 arrivals).
+__device__ __forceinline__ uint32_t bar_owner_go(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 5); }
+__device__ __forceinline__ uint32_t bar_published(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 6); }
+constexpr int kAbortOffset = 8 * (2 * kMaxStages + 7);  // int
 constexpr int kTmemOffset = kAbortOffset + 16;          // uint32
 constexpr int kChunkTabOffset = 256;                    // int4[kMaxSwapChunks]: shard, src_row, valid, out_row
 static_assert(kChunkTabOffset + kMaxSwapChunks * 16 <= kCtlBytes, "control block too small");
@@ -128,43 +132,62 @@ __device__ __forceinline__ void decode_row_tile(const KernelParams& p, int tile,
   nt = r / gm;
 }
 
-struct WorkItem {
-  int mt, nt;    // row tile, n tile
+enum SegRole : int { kSegWhole = 0, kSegOwner = 1, kSegContrib = 2 };
+
+struct Segment {
+  int tile;      // cluster tile
+  int mt, nt;    // this CTA's row tile, n tile
   int kb0, kb1;  // k blocks [kb0, kb1)
-  int part;      // part of a split tail tile (0 = owner)
-  int nparts;    // 1 for a whole tile
-  int tail;      // index of the tail tile, -1 for a whole tile
+  int role;      // whole tile, owner of a split tile, or contributor
 };
 
-// Work item `item` of a cluster: a cluster tile (cluster row mc, n tile nt),
-// whole or one k part of a split tail tile.  CTA `crank` of the cluster takes
-// row tile mc * cm + crank.
-__device__ __forceinline__ WorkItem decode_rows_item(const KernelParams& p, int item, int cm, int crank) {
-  WorkItem w;
-  int tile;
-  if (item < p.full_tiles) {
-    tile = item;
-    w.part = 0;
-    w.nparts = 1;
-    w.tail = -1;
-    w.kb0 = 0;
-    w.kb1 = p.num_k_blocks;
-  } else {
-    const int j = item - p.full_tiles;
-    w.tail = j / p.tail_splits;
-    w.part = j - w.tail * p.tail_splits;
-    w.nparts = p.tail_splits;
-    tile = p.full_tiles + w.tail;
-    w.kb0 = (int)((int64_t)w.part * p.num_k_blocks / w.nparts);
-    w.kb1 = (int)((int64_t)(w.part + 1) * p.num_k_blocks / w.nparts);
-  }
-  decode_row_tile(p, tile, w.mt, w.nt);
-  w.mt = w.mt * cm + crank;
-  return w;
-}
+// The rows-path work of one cluster, in order: its data-parallel tiles, then
+// its contiguous share of the stream-K units (see KernelParams).
+struct SegmentIter {
+  int cid, nclusters, kblocks, dp_tiles, next_dp;
+  int64_t u, hi;
 
-__device__ __forceinline__ void epilogue_bar_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+  __device__ __forceinline__ void init(const KernelParams& p, int cluster_id, int clusters) {
+    cid = cluster_id;
+    nclusters = clusters;
+    kblocks = p.num_k_blocks;
+    dp_tiles = p.dp_tiles;
+    next_dp = cluster_id;
+    const int64_t units = (int64_t)(p.num_tiles - p.dp_tiles) * kblocks;
+    const int64_t base = (int64_t)p.dp_tiles * kblocks;
+    u = base + units * cluster_id / clusters;
+    hi = base + units * (cluster_id + 1) / clusters;
+  }
+
+  __device__ __forceinline__ bool next(const KernelParams& p, int cm, int crank, Segment& s) {
+    if (next_dp < dp_tiles) {
+      s.tile = next_dp;
+      s.kb0 = 0;
+      s.kb1 = kblocks;
+      s.role = kSegWhole;
+      next_dp += nclusters;
+    } else if (u < hi) {
+      const int t = (int)(u / kblocks);
+      s.tile = t;
+      s.kb0 = (int)(u - (int64_t)t * kblocks);
+      const int64_t left = hi - u;
+      s.kb1 = (int)min((int64_t)kblocks, (int64_t)s.kb0 + left);
+      s.role = (s.kb0 == 0) ? (s.kb1 == kblocks ? kSegWhole : kSegOwner) : kSegContrib;
+      u += s.kb1 - s.kb0;
+    } else {
+      return false;
+    }
+    int mc;
+    decode_row_tile(p, s.tile, mc, s.nt);
+    s.mt = mc * cm + crank;
+    return true;
+  }
+};
+
+// First stream-K unit of cluster c.
+__device__ __forceinline__ int64_t sk_first_unit(const KernelParams& p, int c, int clusters) {
+  const int64_t units = (int64_t)(p.num_tiles - p.dp_tiles) * p.num_k_blocks;
+  return (int64_t)p.dp_tiles * p.num_k_blocks + units * c / clusters;
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
@@ -243,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const RingGeom geom = make_ring_geom(p.P, p.m_pd, p.my_id, p.box_rows);
+  const RingGeom geom = make_ring_geom(p.P, p.m_pd, p.my_id, p.box_rows, p.whole_shards);
   const uint64_t limit = p.wait_limit_ns;
 
   if (warp == 0) trace(p, 0);
@@ -257,6 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       ptx::mbar_init(bar_acc_empty(ctl, a), 128);
     }
     ptx::mbar_init(bar_drain(ctl), 1);
+    ptx::mbar_init(bar_owner_go(ctl), 1);
+    ptx::mbar_init(bar_published(ctl), 128);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -298,9 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       (kPath == kPathSwap) ? (int)((int64_t)(split + 1) * p.num_k_blocks / p.splits) : p.num_k_blocks;
   const int crank = (kCM > 1) ? (int)(blockIdx.x % kCM) : 0;  // rank in the cluster
   const uint16_t cmask = (uint16_t)((1u << kCM) - 1u);
-  const int tile_first = (kPath == kPathSwap) ? 0 : (int)(blockIdx.x / kCM);
-  const int tile_step = (kPath == kPathSwap) ? 1 : (int)(gridDim.x / kCM);
-  const int tile_count = (kPath == kPathSwap) ? 1 : p.num_items;
+  const int cluster_id = (int)(blockIdx.x / kCM);
+  const int nclusters = (int)(gridDim.x / kCM);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -314,7 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       uint64_t waited_empty = 0;
       uint64_t* wait_acc = p.trace ? &waited_empty : nullptr;
       const int cpt = kTileM / p.box_rows;
-      for (int tile = tile_first; ok && tile < tile_count; tile += tile_step) {
+      SegmentIter iter;
+      iter.init(p, cluster_id, nclusters);
+      bool swap_pending = true;
+      for (int tile = 0; ok; ++tile) {
         int mt = 0, nt = swap_nt;
         int kb0 = kb_begin, kb1 = kb_end;
         int shard_j[16];
@@ -322,11 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         int nchunks = 0;
         uint32_t bytes;
         if constexpr (kPath == kPathRows) {
-          const WorkItem wi = decode_rows_item(p, tile, kCM, crank);
-          mt = wi.mt;
-          nt = wi.nt;
-          kb0 = wi.kb0;
-          kb1 = wi.kb1;
+          Segment sg;
+          if (!iter.next(p, kCM, crank, sg)) break;
+          mt = sg.mt;
+          nt = sg.nt;
+          kb0 = sg.kb0;
+          kb1 = sg.kb1;
           for (int j = 0; j < cpt; ++j) {
             const int64_t gc = (int64_t)mt * cpt + j;
             if (mt < p.num_m_tiles && gc < p.total_chunks) {
@@ -338,6 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           }
           bytes = (uint32_t)nchunks * p.box_rows * 128u + (uint32_t)kBN * 128u;
         } else {
+          if (!swap_pending) break;
+          swap_pending = false;
           bytes = (uint32_t)kASlotBytes + (uint32_t)p.total_chunks * p.box_rows * 128u;
         }
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -435,7 +465,18 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       uint64_t waited_full = 0, waited_accfree = 0;
       uint64_t* wf = p.trace ? &waited_full : nullptr;
       uint64_t* wa = p.trace ? &waited_accfree : nullptr;
-      for (int tile = tile_first; ok && tile < tile_count; tile += tile_step, ++it) {
+      SegmentIter iter;
+      iter.init(p, cluster_id, nclusters);
+      for (int tile = 0; ok; ++tile, ++it) {
+        int kb0 = kb_begin, kb1 = kb_end;
+        if constexpr (kPath == kPathRows) {
+          Segment sg;
+          if (!iter.next(p, kCM, crank, sg)) break;
+          kb0 = sg.kb0;
+          kb1 = sg.kb1;
+        } else {
+          if (it > 0) break;
+        }
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         int res = wait_phase(bar_acc_empty(ctl, acc), acc_phase ^ 1u, abort_flag, limit, wa);
@@ -445,12 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * mma_n);
-        int kb0 = kb_begin, kb1 = kb_end;
-        if constexpr (kPath == kPathRows) {
-          const WorkItem wi = decode_rows_item(p, tile, kCM, crank);
-          kb0 = wi.kb0;
-          kb1 = wi.kb1;
-        }
         for (int kb = kb0; kb < kb1; ++kb) {
           res = wait_phase(bar_full(ctl, stage), phase, abort_flag, limit, wf);
           if (res != kWaitOk) {
@@ -506,7 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       int it = 0;
       uint64_t waited_accfull = 0;
       uint64_t* we = p.trace ? &waited_accfull : nullptr;
-      for (int tile = tile_first; tile < tile_count; tile += tile_step, ++it) {
+      SegmentIter iter;
+      iter.init(p, cluster_id, nclusters);
+      const size_t slot_floats = (size_t)kTileM * kBN;
+      uint32_t owner_parity = 0, publish_parity = 0;
+      for (int tile = 0;; ++tile, ++it) {
+        Segment sg;
+        if (!iter.next(p, kCM, crank, sg)) break;
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         int res = kWaitOk;
@@ -518,37 +559,56 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         }
         ptx::tc_fence_after();
         if (it == 0) trace(p, 6);
-        const WorkItem wi = decode_rows_item(p, tile, kCM, crank);
-        const int64_t gc = (int64_t)wi.mt * cpt + trow / p.box_rows;
+        const int64_t gc = (int64_t)sg.mt * cpt + trow / p.box_rows;
         const int r = trow % p.box_rows;
         int64_t out_row = -1;
-        if (wi.mt < p.num_m_tiles && gc < p.total_chunks) {
+        if (sg.mt < p.num_m_tiles && gc < p.total_chunks) {
           const RingChunk ch = ring_chunk(geom, gc);
           if (r < ch.valid) out_row = ch.out_row + r;
         }
         const uint32_t tbase = lane_base + (uint32_t)(acc * kBN);
-        // Partial slots of this tail tile: [part-1][BN/32][128 rows][32 floats].
-        const size_t slot_floats = (size_t)kTileM * kBN;
-        const int tail_slot = wi.tail * kCM + crank;
-        float* tail_base = (wi.tail >= 0)
-                               ? p.tail_partials + (size_t)tail_slot * (wi.nparts - 1) * slot_floats
-                               : nullptr;
-        if (wi.nparts > 1 && wi.part == 0) {
-          // Owner: wait (bounded) until the other parts have published.
-          int wres = kWaitOk;
+        // Contributors of an owned tile: the following clusters whose first
+        // stream-K unit falls inside this tile, in k order.
+        int ncontrib = 0;
+        if (sg.role == kSegOwner) {
+          const int64_t tile_end = (int64_t)(sg.tile + 1) * p.num_k_blocks;
+          while (cluster_id + 1 + ncontrib < nclusters &&
+                 sk_first_unit(p, cluster_id + 1 + ncontrib, nclusters) < tile_end)
+            ++ncontrib;
           if (threadIdx.x == 64) {
-            const int* flag = p.tail_flags + tail_slot;
+            int wres = kWaitOk;
+            const int* flag = p.sk_flags + (size_t)(sg.tile - p.dp_tiles) * kCM + crank;
             const uint64_t t0 = ptx::globaltimer_ns();
-            while (ld_acquire_gpu(flag) < wi.nparts - 1) {
+            while (ld_acquire_gpu(flag) < ncontrib) {
               if (*abort_flag) { wres = kWaitAborted; break; }
               if (ptx::globaltimer_ns() - t0 > limit) { wres = kWaitTimeout; break; }
-              __nanosleep(64);
+              __nanosleep(32);
             }
-            if (wres == kWaitOk) *const_cast<volatile int*>(flag) = 0;  // ready for the next run
-            else record_failure(p, abort_flag, wres, kRoleEpilogue, -2, wi.tail);
+            if (wres == kWaitOk) {
+              *const_cast<volatile int*>(flag) = 0;  // ready for the next run
+            } else {
+              record_failure(p, abort_flag, wres, kRoleEpilogue, -2, sg.tile);
+              if (wres == kWaitTimeout && p.status != nullptr && p.status[3] == sg.tile) {
+                p.status[4] = ncontrib;
+                p.status[5] = ld_acquire_gpu(flag);
+                p.status[6] = cluster_id;
+                p.status[7] = crank;
+              }
+            }
+            ptx::mbar_arrive(bar_owner_go(ctl));  // release the other epilogue threads either way
           }
-          epilogue_bar_sync();
+          __syncwarp();
+          int gres = kWaitOk;
+          if (lane == 0) gres = wait_phase(bar_owner_go(ctl), owner_parity, abort_flag, limit);
+          gres = __shfl_sync(0xffffffffu, gres, 0);
+          owner_parity ^= 1u;
+          if (gres != kWaitOk && lane == 0) record_failure(p, abort_flag, gres, kRoleEpilogue, -3, sg.tile);
         }
+        // Partial slot layout [BN/32][8][128 rows][4 floats]: a warp's 16-byte
+        // accesses cover 512 contiguous bytes.
+        float4* my_slot = (sg.role == kSegContrib)
+                              ? reinterpret_cast<float4*>(p.sk_partials + ((size_t)cluster_id * kCM + crank) * slot_floats)
+                              : nullptr;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
@@ -558,36 +618,60 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_acc_empty(ctl, acc));  // TMEM buffer may be reused
           }
-          const size_t row_off = ((size_t)c * kTileM + trow) * 32;
-          if (wi.nparts > 1 && wi.part > 0) {
-            float4* dst = reinterpret_cast<float4*>(tail_base + (size_t)(wi.part - 1) * slot_floats + row_off);
+          if (sg.role == kSegContrib) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-          } else {
-            if (wi.nparts > 1) {
-              // own partial + part 1 + part 2 + ... in this fixed order
-              for (int pp = 1; pp < wi.nparts; ++pp) {
-                const float4* src = reinterpret_cast<const float4*>(tail_base + (size_t)(pp - 1) * slot_floats + row_off);
+              my_slot[((size_t)c * 8 + i) * kTileM + trow] =
+                  make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                              __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            continue;
+          }
+          // Owner: own partial + contributor 1 + contributor 2 + ... (k order);
+          // two contributors' loads are in flight together.
+          for (int j = 0; j < ncontrib; j += 2) {
+            const float4* s0 = reinterpret_cast<const float4*>(
+                p.sk_partials + ((size_t)(cluster_id + 1 + j) * kCM + crank) * slot_floats);
+            const float4* s1 = reinterpret_cast<const float4*>(
+                p.sk_partials + ((size_t)(cluster_id + 2 + j) * kCM + crank) * slot_floats);
+            float4 q0[8], q1[8];
+            const bool two = j + 1 < ncontrib;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float4 q4 = __ldcg(src + i);
-                  v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) + q4.x);
-                  v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + q4.y);
-                  v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + q4.z);
-                  v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + q4.w);
-                }
+            for (int i = 0; i < 8; ++i) {
+              q0[i] = __ldcg(s0 + ((size_t)c * 8 + i) * kTileM + trow);
+              if (two) q1[i] = __ldcg(s1 + ((size_t)c * 8 + i) * kTileM + trow);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) + q0[i].x);
+              v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + q0[i].y);
+              v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + q0[i].z);
+              v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + q0[i].w);
+            }
+            if (two) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) + q1[i].x);
+                v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + q1[i].y);
+                v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + q1[i].z);
+                v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + q1[i].w);
               }
             }
-            if (out_row >= 0) store_row32<kF32>(p.out, p.ldo, out_row, (int64_t)wi.nt * kBN + c * 32, v);
           }
+          if (out_row >= 0) store_row32<kF32>(p.out, p.ldo, out_row, (int64_t)sg.nt * kBN + c * 32, v);
         }
-        if (wi.nparts > 1 && wi.part > 0) {
-          // Publish: every thread's stores, then one arrival for the tile.
+        if (sg.role == kSegContrib) {
+          // Publish: every thread fences its stores and arrives; one thread
+          // waits for all 128 and counts the partial for the owner.
           __threadfence();
-          epilogue_bar_sync();
-          if (threadIdx.x == 64) atomicAdd(p.tail_flags + tail_slot, 1);
+          ptx::mbar_arrive(bar_published(ctl));
+          if (threadIdx.x == 64) {
+            const int pres = wait_phase(bar_published(ctl), publish_parity, abort_flag, limit);
+            if (pres == kWaitOk)
+              atomicAdd(p.sk_flags + (size_t)(sg.tile - p.dp_tiles) * kCM + crank, 1);
+            else
+              record_failure(p, abort_flag, pres, kRoleEpilogue, -4, sg.tile);
+          }
+          publish_parity ^= 1u;
         }
       }
       trace(p, 7);

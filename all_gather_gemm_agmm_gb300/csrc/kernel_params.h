@@ -37,6 +37,7 @@ struct __align__(64) KernelParams {
   int my_id;
   int box_rows;                  // rows per chunk (a power of two, 8..128)
   int box_shift;                 // log2(box_rows)
+  int whole_shards;              // chunks cover whole shards in ring first-visit order
   int total_chunks;              // chunks in the ring-ordered row sequence
   int num_m_tiles;               // row path: 128-row tiles of chunks
   int num_mc_tiles;              // row path: cluster rows = ceil(num_m_tiles / CTAs per cluster)
@@ -52,17 +53,18 @@ struct __align__(64) KernelParams {
   uint64_t wait_limit_ns;        // bound on every mbarrier wait
   int test_drop_first_arrive;    // test hook: producer skips its first arrival
   uint64_t* trace;               // optional [CTAs][kTraceSlots] timestamps (null: off)
-  // Rows path work items: tiles [0, full_tiles) whole, then each of the
-  // remaining (tail) tiles split into tail_splits k-ranges.  Part 0 of a
-  // tail tile owns it: the other parts leave float32 partials in
-  // tail_partials and count themselves in tail_flags[tail]; the owner waits
-  // for tail_splits-1 arrivals, adds the partials in part order and resets the
-  // counter to 0.
-  int full_tiles;
-  int tail_splits;
-  int num_items;
-  int* tail_flags;               // [tail tiles][cluster rank] arrival counters (zero between runs)
-  float* tail_partials;          // [tail tiles][cluster rank][tail_splits-1][BN/32][128][32]
+  // Rows path work (hybrid stream-K).  Cluster tiles [0, dp_tiles) are dealt
+  // round-robin to the clusters whole.  The k blocks of the remaining tiles
+  // (sk units) are divided evenly: cluster c takes units [c*U/C, (c+1)*U/C).
+  // A tile's k blocks may so be spread over consecutive clusters: the one
+  // holding k block 0 owns the tile; the others (contributors) each leave a
+  // float32 partial in sk_partials[cluster][cluster rank] and count themselves
+  // in sk_flags[tile - dp_tiles][cluster rank].  The owner waits for them,
+  // adds the partials in k order and resets the counter to 0.
+  int dp_tiles;
+  int sk_min_units;              // unused on the device; planner bookkeeping
+  int* sk_flags;                 // [sk tiles][cluster rank] arrival counters (zero between runs)
+  float* sk_partials;            // [clusters][cluster rank][BN/32][8][128][4]
 };
 
 struct GatherParams {

@@ -16,6 +16,11 @@
 // which row chunks are visited: step 0 takes shard my_id, step s the left half
 // of shard (my_id+s) mod P and the right half of shard (my_id-s) mod P.  Each
 // half is cut into chunks of box_rows rows (the last one ragged).
+//
+// Whole-shard mode (for shards whose halves are too small to fill a TMA box)
+// keeps the ring's shard order at shard granularity: shards in the order the
+// bidirectional ring first delivers them -- my_id, my_id+1, my_id-1, my_id+2,
+// my_id-2, ... (mod P) -- each cut into chunks of box_rows rows.
 #pragma once
 
 #include <stdint.h>
@@ -35,7 +40,8 @@ struct RingGeom {
   int chunks_l;   // chunks in a left half  = ceil(half_l / box_rows)
   int chunks_r;   // chunks in a right half = ceil(half_r / box_rows)
   int64_t m_pd;   // rows per shard
-  int64_t half_l; // m_pd / 2 (floor): m_per_device_per_direction
+  int64_t half_l; // m_pd / 2 (floor): m_per_device_per_direction; 0 in whole-shard mode
+  int whole;      // whole-shard mode
 };
 
 struct RingChunk {
@@ -47,16 +53,24 @@ struct RingChunk {
 
 AGMM_HD int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-AGMM_HD RingGeom make_ring_geom(int P, int64_t m_pd, int my_id, int box_rows) {
+AGMM_HD RingGeom make_ring_geom(int P, int64_t m_pd, int my_id, int box_rows, int whole = 0) {
   RingGeom g;
   g.P = P;
   g.my_id = my_id;
   g.box_rows = box_rows;
   g.m_pd = m_pd;
-  g.half_l = m_pd / 2;
+  g.whole = whole;
+  g.half_l = whole ? 0 : m_pd / 2;
   g.chunks_l = (int)ceil_div64(g.half_l, box_rows);
   g.chunks_r = (int)ceil_div64(m_pd - g.half_l, box_rows);
   return g;
+}
+
+// Offset of the t-th shard the bidirectional ring delivers: 0, +1, -1, +2, ...
+AGMM_HD int ring_first_visit(int my_id, int t, int P) {
+  const int off = (t & 1) ? (t + 1) / 2 : -(t / 2);
+  int s = (my_id + off) % P;
+  return s < 0 ? s + P : s;
 }
 
 AGMM_HD int64_t ring_total_chunks(const RingGeom& g) {
@@ -72,7 +86,11 @@ AGMM_HD RingChunk ring_chunk(const RingGeom& g, int64_t c64) {
   const int w = c - s * per_step;
   RingChunk ch;
   int64_t seg_end;
-  if (w < g.chunks_l) {
+  if (g.whole) {
+    ch.shard = ring_first_visit(g.my_id, s, g.P);
+    ch.src_row = (int64_t)w * g.box_rows;
+    seg_end = g.m_pd;
+  } else if (w < g.chunks_l) {
     ch.shard = g.my_id + s;
     if (ch.shard >= g.P) ch.shard -= g.P;
     ch.src_row = (int64_t)w * g.box_rows;

@@ -308,6 +308,9 @@ def bench_ours(args, w):
     ws = plan.new_workspace(False, device=device)
     ws_unf = plan.new_workspace(True, device=device)
     stream = torch.cuda.Stream(device=device)
+    # inputs and zeroed workspaces come from the current stream; the kernels
+    # run on `stream`
+    torch.cuda.synchronize()
 
     def fused_step(rep):
         xs, y, o = rep
@@ -427,6 +430,7 @@ def bench_sweep(args):
         plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose)
         ws = plan.new_workspace(False, device=device)
         wsu = plan.new_workspace(True, device=device)
+        torch.cuda.synchronize()  # zeroed workspaces and inputs before launches on `stream`
         fused = [(lambda rep: (lambda s: plan.run(rep[0], rep[1], rep[2], w.my_id, ws, s)))(r) for r in reps]
         unf = [(lambda rep: (lambda s: plan.run_unfused(rep[0], rep[1], rep[2], w.my_id, wsu, s)))(r) for r in reps]
         g1 = time_graph(fused, 0, 3, stream)

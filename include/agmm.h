@@ -68,6 +68,8 @@ typedef struct {
   int path;          /* 0: row tiles (MMA M spans gathered rows);
                         1: swapped tiles (MMA M spans n, gathered rows are MMA N) */
   int box_rows;      /* rows per X tensor-map box (a "chunk")                    */
+  int whole_shards;  /* 0: chunks follow the ring's left/right half split;
+                        1: chunks cover whole shards in ring first-visit order   */
   int chunks;        /* chunks in the whole ring-ordered row sequence            */
   int tile_m;        /* MMA M                                                    */
   int tile_n;        /* MMA N                                                    */
@@ -208,13 +210,18 @@ agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info);
  * The ring-ordered row sequence, host side (no device needed).  For box
  * height box_rows the sequence is cut into chunks; chunk c covers rows
  * [src_row[c], src_row[c] + valid[c]) of shard shard[c], which land at rows
- * [out_row[c], out_row[c] + valid[c]) of O.  Chunks follow ring step s = 0..P-1,
- * left half of shard (my_id+s) mod P then right half of shard (my_id-s) mod P.
- * Writes at most max_chunks entries and stores the full count in *n_chunks.
+ * [out_row[c], out_row[c] + valid[c]) of O.  With whole_shards == 0 chunks
+ * follow ring step s = 0..P-1: left half of shard (my_id+s) mod P, then right
+ * half of shard (my_id-s) mod P.  With whole_shards == 1 each shard is one
+ * run of chunks, shards in the order the bidirectional ring first delivers
+ * them: my_id, my_id+1, my_id-1, my_id+2, ... (mod P); the planner uses this
+ * when the halves are too small to fill a TMA box.  Writes at most max_chunks
+ * entries and stores the full count in *n_chunks.
  */
 agmm_status_t agmm_ring_chunks(int P, int64_t m_per_device, int my_id, int box_rows,
-                               int32_t* shard, int64_t* src_row, int64_t* out_row,
-                               int32_t* valid, int64_t max_chunks, int64_t* n_chunks);
+                               int whole_shards, int32_t* shard, int64_t* src_row,
+                               int64_t* out_row, int32_t* valid, int64_t max_chunks,
+                               int64_t* n_chunks);
 
 /* Static description of a status code. */
 const char* agmm_status_string(agmm_status_t status);

@@ -86,13 +86,16 @@ def test_valid_shape_without_device_is_a_cuda_error(agmm_lib):
 def test_ring_chunks_argument_checks(agmm_lib):
     n = ctypes.c_int64(0)
     f = agmm_lib.agmm_ring_chunks
-    assert f(0, 4, 0, 8, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_ERR_INVALID_ARG
-    assert f(2, 4, 2, 8, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_ERR_INVALID_ARG
-    assert f(2, 0, 0, 8, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_ERR_INVALID_ARG
-    assert f(2, 4, 0, 0, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_ERR_INVALID_ARG
-    assert f(2, 4, 0, 8, None, None, None, None, 0, None) == agmm.AGMM_ERR_INVALID_ARG
-    assert f(2, 4, 0, 8, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_OK
+    assert f(0, 4, 0, 8, 0, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_ERR_INVALID_ARG
+    assert f(2, 4, 2, 8, 0, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_ERR_INVALID_ARG
+    assert f(2, 0, 0, 8, 0, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_ERR_INVALID_ARG
+    assert f(2, 4, 0, 0, 0, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_ERR_INVALID_ARG
+    assert f(2, 4, 0, 8, 2, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_ERR_INVALID_ARG
+    assert f(2, 4, 0, 8, 0, None, None, None, None, 0, None) == agmm.AGMM_ERR_INVALID_ARG
+    assert f(2, 4, 0, 8, 0, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_OK
     assert n.value == 2 * 2
+    assert f(2, 4, 0, 8, 1, None, None, None, None, 0, ctypes.byref(n)) == agmm.AGMM_OK
+    assert n.value == 2
 
 
 def test_missing_library_fails_loudly(tmp_path):

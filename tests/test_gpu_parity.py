@@ -131,30 +131,30 @@ def test_parity_full_size_sampled_rows(agmm, name):
     assert bool(torch.isfinite(o.float()).all())
 
 
-@pytest.mark.parametrize("tail", ["1", "2", "3", "8"])
-def test_tail_split_parts(agmm, tail, monkeypatch):
-    # The last partial wave of row tiles is split along k into parts whose
-    # float32 partials the owning part adds in a fixed order.
-    monkeypatch.setenv("AGMM_TAIL_SPLIT", tail)
-    for (P, m, k, n, rt) in [(5, 77, 1024, 256, False), (3, 200, 2048, 384, True)]:
+@pytest.mark.parametrize("streamk", ["0", "1"])
+def test_stream_k_split(agmm, streamk, monkeypatch):
+    # Tiles beyond the last whole wave are spread over the clusters by k
+    # blocks; owners add the contributors' float32 partials in k order.
+    monkeypatch.setenv("AGMM_STREAMK", streamk)
+    for (P, m, k, n, rt) in [(5, 77, 1024, 256, False), (3, 200, 2048, 384, True), (8, 260, 768, 1280, False)]:
         xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=4)
         ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
         o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=1)
-        check(o, ref32, f"tail split {tail} {plan.info()}")
-        # a second run reuses the zeroed counters
+        check(o, ref32, f"stream-k {streamk} {plan.info()}")
+        # a second run reuses the counters the owners reset
         o2, _ = _run(agmm, xs_cpu, y_cpu, rt, my_id=1, plan=plan)
         assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
 
 
 @pytest.mark.parametrize("case", [(3, 200, 1024, 512, False), (5, 300, 512, 256, True), (8, 130, 256, 640, True)])
 def test_cluster_multicast_matches_single_cta(agmm, case, monkeypatch):
-    # Pairs of CTAs share each Y tile through TMA multicast; with no tail split
+    # Pairs of CTAs share each Y tile through TMA multicast; without stream-K
     # the arithmetic is unchanged, so the output is bitwise equal to one CTA
     # per cluster.  Odd row-tile counts exercise the idle second CTA.
     P, m, k, n, rt = case
     xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=6)
     ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
-    monkeypatch.setenv("AGMM_TAIL_SPLIT", "1")
+    monkeypatch.setenv("AGMM_STREAMK", "0")
     outs = {}
     for cm in ("1", "2"):
         monkeypatch.setenv("AGMM_CM", cm)
@@ -162,3 +162,20 @@ def test_cluster_multicast_matches_single_cta(agmm, case, monkeypatch):
         check(o, ref32, f"cm={cm} {plan.info()}")
         outs[cm] = o
     assert torch.equal(outs["1"].view(torch.int16), outs["2"].view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", ["half", "whole"])
+@pytest.mark.parametrize("case", [(2, 16, 256, 128, False, "uniform"), (4, 64, 1024, 1024, True, "normal"),
+                                  (8, 8, 512, 256, False, "normal"), (3, 13, 256, 256, True, "normal"),
+                                  (8, 128, 512, 512, True, "normal"), (3, 200, 512, 384, False, "normal")],
+                         ids=lambda c: "P{}_m{}".format(c[0], c[1]) if isinstance(c, tuple) else c)
+def test_chunking_modes(agmm, case, mode, monkeypatch):
+    # Half-shard chunks follow the ring's left/right split; whole-shard chunks
+    # follow the ring's first-visit shard order.  Both give the same product.
+    monkeypatch.setenv("AGMM_CHUNKS", mode)
+    P, m, k, n, rt, dist = case
+    xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, dist=dist, seed=8)
+    ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+    o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=P // 2)
+    assert plan.info()["whole_shards"] == (mode == "whole")
+    check(o, ref32, f"{mode} {plan.info()}")

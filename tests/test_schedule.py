@@ -12,8 +12,8 @@ import pytest
 import all_gather_gemm_agmm_gb300 as agmm
 
 
-def chunks(P, m, my_id, bh):
-    return agmm.ring_chunks(P, m, my_id, bh)
+def chunks(P, m, my_id, bh, whole=False):
+    return agmm.ring_chunks(P, m, my_id, bh, whole)
 
 
 def halves_in_order(ch):
@@ -47,11 +47,12 @@ def test_matches_pallas_output_offsets(agmm_lib, P):
                 assert sum(t[3] for t in left) == h and sum(t[3] for t in right) == m - h
 
 
+@pytest.mark.parametrize("whole", [False, True])
 @pytest.mark.parametrize("P,m,bh", [(1, 1, 8), (1, 7, 8), (2, 16, 8), (3, 5, 8), (4, 64, 32), (8, 1000, 128),
                                     (8, 1000, 8), (5, 333, 16), (8, 4096, 128), (7, 129, 64), (2, 3, 128)])
-def test_every_row_exactly_once(agmm_lib, P, m, bh):
+def test_every_row_exactly_once(agmm_lib, P, m, bh, whole):
     for my_id in range(P):
-        ch = chunks(P, m, my_id, bh)
+        ch = chunks(P, m, my_id, bh, whole)
         seen = {}
         for s, r0, o0, v in zip(ch["shard"], ch["src_row"], ch["out_row"], ch["valid"]):
             assert 1 <= v <= bh
@@ -80,3 +81,19 @@ def test_odd_and_single_row_shards(agmm_lib):
     assert ch["shard"] == [2, 1, 0]
     ch = chunks(2, 5, 0, 8)  # left 2 rows, right 3 rows
     assert list(zip(ch["src_row"], ch["valid"])) == [(0, 2), (2, 3), (0, 2), (2, 3)]
+
+
+@pytest.mark.parametrize("P", range(1, 9))
+def test_whole_shard_first_visit_order(agmm_lib, P):
+    # Whole shards in the order the bidirectional ring first delivers them:
+    # step 0 my_id, step s the shards my_id+s (left halves) and my_id-s (right).
+    for my_id in range(P):
+        ch = chunks(P, 10, my_id, 8, whole=True)
+        order = [s for s, r0 in zip(ch["shard"], ch["src_row"]) if r0 == 0]
+        want, seen = [], set()
+        for s in range(P):
+            for shard in ((my_id + s) % P, (my_id - s) % P):
+                if shard not in seen:
+                    seen.add(shard)
+                    want.append(shard)
+        assert order == want
