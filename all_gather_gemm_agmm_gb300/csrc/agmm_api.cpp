@@ -353,8 +353,12 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
     const int T = pl->num_tiles;
     int dp = T;
     if (T % G != 0 && env_int("AGMM_STREAMK", 1) != 0) {
+      // Stream-K over the ragged last wave alone keeps its tiles together in
+      // raster order (L2 reuse) as long as a tile is shared by at most about
+      // three clusters; a thinner last wave also takes the wave before it.
       const int W = T / G;
-      dp = W >= 1 ? (W - 1) * G : 0;
+      const int R = T - W * G;
+      dp = (W >= 1 && 3 * R >= G) ? W * G : (W >= 1 ? (W - 1) * G : 0);
       // at least 4 k blocks per cluster share
       const int64_t units = (int64_t)(T - dp) * pl->num_k_blocks;
       if (units < (int64_t)G * 4) G = (int)std::max<int64_t>(1, units / 4);
