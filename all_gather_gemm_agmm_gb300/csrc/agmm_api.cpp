@@ -180,6 +180,7 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->key.path = kPathSwap;
     pl->key.bn = kTileM;
     pl->key.cm = 1;
+    pl->key.pair = false;
     pl->box_rows = best_bh;
     pl->whole_shards = best_whole;
     pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, best_bh, best_whole));
@@ -241,12 +242,18 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     const int env_cm = env_int("AGMM_CM", 0);
     if (env_cm == 1 || env_cm == 2) cm = env_cm;
     pl->key.cm = cm;
+    // Two-CTA clusters either multiply alone with the Y tile multicast (the
+    // default) or, with AGMM_PAIR=1, as a cta_group::2 pair in which each CTA
+    // holds its 128 rows and half the Y tile (32 KiB per k block and SM instead
+    // of 48 KiB).  On GB300 the pair measured no faster for Y stored [n, k] and
+    // slower for Y stored [k, n], so it stays opt-in.
+    pl->key.pair = cm == 2 && env_int("AGMM_PAIR", 0) != 0;
     pl->num_mc_tiles = (pl->num_m_tiles + cm - 1) / cm;
     if ((int64_t)pl->num_mc_tiles * pl->num_n_tiles > ((int64_t)1 << 31) - 1)
       return fail(AGMM_ERR_INVALID_ARG, "too many output tiles");
     pl->num_tiles = pl->num_mc_tiles * pl->num_n_tiles;
     pl->mma_n = bn;
-    pl->b_slot_bytes = (uint32_t)bn * 128u;
+    pl->b_slot_bytes = (uint32_t)(pl->key.pair ? bn / 2 : bn) * 128u;
     const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
     pl->stages = (int)std::min<int64_t>(kMaxStages, budget / stage_bytes);
     pl->stages = std::min(pl->stages, std::max(2, env_int("AGMM_STAGES", kMaxStages)));

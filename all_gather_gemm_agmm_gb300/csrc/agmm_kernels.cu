@@ -56,21 +56,35 @@ __device__ __forceinline__ uint32_t bar_drain(uint32_t ctl) {
 // (1 arrival) and the contributors' "partial stored" (128 arrivals).
 __device__ __forceinline__ uint32_t bar_owner_go(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 5); }
 __device__ __forceinline__ uint32_t bar_published(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 6); }
-constexpr int kAbortOffset = 8 * (2 * kMaxStages + 7);  // int
+// CTA pairs: the follower's "stage s landed" forwarded to the leader.
+__device__ __forceinline__ uint32_t bar_peer_full(uint32_t ctl, int s) {
+  return ctl + 8u * (2 * kMaxStages + 7 + s);
+}
+constexpr int kAbortOffset = 8 * (3 * kMaxStages + 7);  // int
 constexpr int kTmemOffset = kAbortOffset + 16;          // uint32
-constexpr int kChunkTabOffset = 256;                    // int4[kMaxSwapChunks]: shard, src_row, valid, out_row
+constexpr int kChunkTabOffset = 512;                    // int4[kMaxSwapChunks]: shard, src_row, valid, out_row
+static_assert(kTmemOffset + 4 <= kChunkTabOffset, "control block overlap");
 static_assert(kChunkTabOffset + kMaxSwapChunks * 16 <= kCtlBytes, "control block too small");
 
 enum WaitResult : int { kWaitOk = 1, kWaitTimeout = 0, kWaitAborted = -1 };
 
 // Bounded wait for the phase of `bar` with the given parity.  When `waited`
 // is given, the time spent blocked is added to it (trace only).
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+  if constexpr (kClusterScope)
+    return ptx::mbar_try_wait_cluster(bar, parity);
+  else
+    return ptx::mbar_try_wait(bar, parity);
+}
+
+template <bool kClusterScope = false>
 __device__ __forceinline__ int wait_phase(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns, uint64_t* waited = nullptr) {
-  if (ptx::mbar_try_wait(bar, parity)) return kWaitOk;
+  if (try_wait_scoped<kClusterScope>(bar, parity)) return kWaitOk;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) {
+    if (try_wait_scoped<kClusterScope>(bar, parity)) {
       if (waited) *waited += ptx::globaltimer_ns() - t0;
       return kWaitOk;
     }
@@ -248,9 +262,14 @@ __device__ __forceinline__ void store_row4(void* out, int64_t ldo, int64_t row, 
 // (K-major tiles); otherwise Y is [k, n] and its tiles are MN-major.  kF32:
 // float32 output.  kBN: n tile of the rows path (the swap path uses 128).
 // ----------------------------------------------------------------------------
-template <int kPath, bool kYK, bool kF32, int kBN, int kCM>
+template <int kPath, bool kYK, bool kF32, int kBN, int kCM, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_constant__ KernelParams p) {
   static_assert(kCM == 1 || (kPath == kPathRows && (kYK || kBN / 64 >= kCM)), "bad cluster multicast shape");
+  static_assert(!kPair || (kCM == 2 && kPath == kPathRows), "CTA pairs are clusters of two on the rows path");
+  // The leader's accumulator-release barrier receives the follower's
+  // epilogue arrivals (release at cluster scope): its wait acquires at
+  // cluster scope.  Stage barriers are fed by TMA and tcgen05.commit.
+  constexpr bool kCS = kPair;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -272,12 +291,16 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   if (warp == 0) trace(p, 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(bar_full(ctl, s), 1);
-      ptx::mbar_init(bar_empty(ctl, s), kCM);  // every cluster CTA's MMA frees the stage
+      // a pair: both producers count their bytes on the leader's barrier
+      ptx::mbar_init(bar_full(ctl, s), kPair ? 2 : 1);
+      // every cluster CTA's MMA frees the stage (a pair: the leader's MMA alone)
+      ptx::mbar_init(bar_empty(ctl, s), kPair ? 1 : kCM);
+      ptx::mbar_init(bar_peer_full(ctl, s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_acc_full(ctl, a), 1);
-      ptx::mbar_init(bar_acc_empty(ctl, a), 128);
+      // a pair: both CTAs' epilogues drain the accumulator the leader fills
+      ptx::mbar_init(bar_acc_empty(ctl, a), kPair ? 256 : 128);
     }
     ptx::mbar_init(bar_drain(ctl), 1);
     ptx::mbar_init(bar_owner_go(ctl), 1);
@@ -298,8 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     }
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), (uint32_t)p.tmem_cols);
-    ptx::tmem_relinquish();
+    if constexpr (kPair) {
+      ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), (uint32_t)p.tmem_cols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_addr(tmem_slot), (uint32_t)p.tmem_cols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -364,7 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
               ++nchunks;
             }
           }
-          bytes = (uint32_t)nchunks * p.box_rows * 128u + (uint32_t)kBN * 128u;
+          // a pair CTA receives only its half of the Y tile
+          bytes = (uint32_t)nchunks * p.box_rows * 128u + (uint32_t)(kPair ? kBN / 2 : kBN) * 128u;
         } else {
           if (!swap_pending) break;
           swap_pending = false;
@@ -377,20 +406,31 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             ok = false;
             break;
           }
-          const uint32_t full = bar_full(ctl, stage);
+          // A pair follower's copies complete on the leader's barrier.
+          const bool to_leader = kPair && crank == 1;
+          const uint32_t full = to_leader ? ptx::map_shared_rank(bar_full(ctl, stage), 0) : bar_full(ctl, stage);
           if (p.test_drop_first_arrive && !dropped) {
             dropped = true;  // the MMA thread's wait on this stage runs out
           } else {
-            ptx::mbar_arrive_expect_tx(full, bytes);
-            armed |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            if (to_leader) {
+              ptx::mbar_arrive_expect_tx_remote(full, bytes);
+            } else {
+              ptx::mbar_arrive_expect_tx(full, bytes);
+              armed |= 1u << stage;
+              armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            }
             const uint32_t a_dst = a0 + (uint32_t)stage * kASlotBytes;
             const uint32_t b_dst = b0 + (uint32_t)stage * p.b_slot_bytes;
             const int k0 = kb * kTileK;
             if constexpr (kPath == kPathRows) {
-              for (int j = 0; j < nchunks; ++j)
-                ptx::tma_load_2d(a_dst + (uint32_t)j * p.box_rows * 128u, &p.xmap[shard_j[j]], full,
-                                 k0, row_j[j]);
+              for (int j = 0; j < nchunks; ++j) {
+                if (to_leader)
+                  ptx::tma_load_2d_pair(a_dst + (uint32_t)j * p.box_rows * 128u, &p.xmap[shard_j[j]], full, k0,
+                                        row_j[j]);
+                else
+                  ptx::tma_load_2d(a_dst + (uint32_t)j * p.box_rows * 128u, &p.xmap[shard_j[j]], full, k0,
+                                   row_j[j]);
+              }
               if constexpr (kCM == 1) {
                 if constexpr (kYK) {
                   ptx::tma_load_2d(b_dst, &p.ymap, full, k0, nt * kBN);
@@ -398,6 +438,25 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
 #pragma unroll
                   for (int a = 0; a < kBN / 64; ++a)
                     ptx::tma_load_2d(b_dst + (uint32_t)a * 8192u, &p.ymap, full, nt * kBN + a * 64, k0);
+                }
+              } else if constexpr (kPair) {
+                // This CTA's half of the Y tile's N rows, into its own slot.
+                if constexpr (kYK) {
+                  if (to_leader)
+                    ptx::tma_load_2d_pair(b_dst, &p.ymap, full, k0, nt * kBN + crank * (kBN / 2));
+                  else
+                    ptx::tma_load_2d(b_dst, &p.ymap, full, k0, nt * kBN + crank * (kBN / 2));
+                } else {
+                  constexpr int kBoxes = kBN / 64 / 2;
+#pragma unroll
+                  for (int aa = 0; aa < kBoxes; ++aa) {
+                    if (to_leader)
+                      ptx::tma_load_2d_pair(b_dst + (uint32_t)aa * 8192u, &p.ymap, full,
+                                            nt * kBN + (crank * kBoxes + aa) * 64, k0);
+                    else
+                      ptx::tma_load_2d(b_dst + (uint32_t)aa * 8192u, &p.ymap, full,
+                                       nt * kBN + (crank * kBoxes + aa) * 64, k0);
+                  }
                 }
               } else {
                 // This CTA's share of the Y tile, multicast to the whole cluster.
@@ -451,13 +510,18 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (kPair && crank == 1) {
+      // Pair follower: the leader's MMA thread works for both CTAs; the
+      // follower's copies complete on the leader's stage barriers.
+    } else if (lane == 0) {
       constexpr int kN = (kPath == kPathRows) ? kBN : 0;
       const int mma_n = (kPath == kPathRows) ? kN : p.mma_n;
       // rows path: A = X chunks (K-major), B = Y; swap path: A = Y, B = X chunks.
       const bool a_mn = (kPath == kPathSwap) && !kYK;
       const bool b_mn = (kPath == kPathRows) && !kYK;
-      const uint32_t idesc = ptx::idesc_bf16_f32(kTileM, mma_n, a_mn, b_mn);
+      // a pair MMA spans both CTAs' 128 rows: M = 256
+      const uint32_t idesc = ptx::idesc_bf16_f32(kPair ? 2 * kTileM : kTileM, mma_n, a_mn, b_mn);
+      constexpr uint16_t kPairMask = 3;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -479,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         }
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-        int res = wait_phase(bar_acc_empty(ctl, acc), acc_phase ^ 1u, abort_flag, limit, wa);
+        int res = wait_phase<kCS>(bar_acc_empty(ctl, acc), acc_phase ^ 1u, abort_flag, limit, wa);
         if (res != kWaitOk) {
           record_failure(p, abort_flag, res, kRoleMma, -1, tile);
           break;
@@ -487,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * mma_n);
         for (int kb = kb0; kb < kb1; ++kb) {
+          // (a pair: this barrier also counts the follower's copies)
           res = wait_phase(bar_full(ctl, stage), phase, abort_flag, limit, wf);
           if (res != kWaitOk) {
             record_failure(p, abort_flag, res, kRoleMma, stage, tile);
@@ -507,11 +572,16 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             const uint64_t b_desc =
                 b_mn ? ptx::smem_desc_sw128(b_addr + kk * 2048u, 8192u, 1024u)
                      : ptx::smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
-            ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            if constexpr (kPair)
+              ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            else
+              ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           // frees the stage (in every cluster CTA: their producers multicast
           // into it) once these MMAs finish
-          if constexpr (kCM > 1)
+          if constexpr (kPair)
+            ptx::mma_commit_pair(bar_empty(ctl, stage), kPairMask);
+          else if constexpr (kCM > 1)
             ptx::mma_commit_multicast(bar_empty(ctl, stage), cmask);
           else
             ptx::mma_commit(bar_empty(ctl, stage));
@@ -521,13 +591,20 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           }
         }
         if (!ok) break;
-        ptx::mma_commit(bar_acc_full(ctl, acc));  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs of a pair)
+        if constexpr (kPair)
+          ptx::mma_commit_pair(bar_acc_full(ctl, acc), kPairMask);
+        else
+          ptx::mma_commit(bar_acc_full(ctl, acc));
       }
       trace(p, 5);
       trace_value(p, 14, waited_full);
       trace_value(p, 15, waited_accfree);
       // Every MMA this thread issued has finished once the drain barrier fires.
-      ptx::mma_commit(bar_drain(ctl));
+      if constexpr (kPair)
+        ptx::mma_commit_pair(bar_drain(ctl), kPairMask);
+      else
+        ptx::mma_commit(bar_drain(ctl));
       if (!wait_drain(bar_drain(ctl), 0, limit))
         record_failure(p, abort_flag, kWaitTimeout, kRoleDrain, -1, -1);
     }
@@ -616,7 +693,11 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           ptx::tmem_ld_wait();
           if (c == kBN / 32 - 1) {
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_acc_empty(ctl, acc));  // TMEM buffer may be reused
+            // TMEM buffer may be reused (a pair's leader refills both CTAs')
+            if (kPair && crank == 1)
+              ptx::mbar_arrive_remote(ptx::map_shared_rank(bar_acc_empty(ctl, acc), 0));
+            else
+              ptx::mbar_arrive(bar_acc_empty(ctl, acc));
           }
           if (sg.role == kSegContrib) {
 #pragma unroll
@@ -804,7 +885,10 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   if (warp == 0) trace(p, 11);
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+    if constexpr (kPair)
+      ptx::tmem_dealloc_pair(tmem_base, (uint32_t)p.tmem_cols);
+    else
+      ptx::tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
   }
 }
 
@@ -834,18 +918,24 @@ __global__ void __launch_bounds__(256) agmm_gather_rows(const __grid_constant__ 
 using KernelFn = void (*)(KernelParams);
 
 KernelFn select_kernel(const KernelKey& k) {
-#define AGMM_PICK(PATH, BN, CM)                                                              \
-  (k.y_kmajor ? (k.out_f32 ? &agmm_fused_sm103a<PATH, true, true, BN, CM>                    \
-                           : &agmm_fused_sm103a<PATH, true, false, BN, CM>)                  \
-              : (k.out_f32 ? &agmm_fused_sm103a<PATH, false, true, BN, CM>                   \
-                           : &agmm_fused_sm103a<PATH, false, false, BN, CM>))
-  if (k.path == kPathSwap) return k.cm == 1 ? AGMM_PICK(kPathSwap, 128, 1) : nullptr;
+#define AGMM_PICK(PATH, BN, CM, PAIR)                                                        \
+  (k.y_kmajor ? (k.out_f32 ? &agmm_fused_sm103a<PATH, true, true, BN, CM, PAIR>              \
+                           : &agmm_fused_sm103a<PATH, true, false, BN, CM, PAIR>)            \
+              : (k.out_f32 ? &agmm_fused_sm103a<PATH, false, true, BN, CM, PAIR>             \
+                           : &agmm_fused_sm103a<PATH, false, false, BN, CM, PAIR>))
+  if (k.path == kPathSwap) return (k.cm == 1 && !k.pair) ? AGMM_PICK(kPathSwap, 128, 1, false) : nullptr;
   if (k.cm == 1) {
-    if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 1);
-    if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 1);
+    if (k.pair) return nullptr;
+    if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 1, false);
+    if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 1, false);
   } else if (k.cm == 2) {
-    if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2);
-    if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2);
+    if (k.pair) {
+      if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2, true);
+      if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2, true);
+    } else {
+      if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2, false);
+      if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2, false);
+    }
   }
   return nullptr;
 #undef AGMM_PICK

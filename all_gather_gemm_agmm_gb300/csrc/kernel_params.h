@@ -80,7 +80,9 @@ struct KernelKey {
   bool y_kmajor;
   bool out_f32;
   int bn;
-  int cm;  // row path: CTAs per cluster along M sharing each Y tile by TMA multicast
+  int cm;     // row path: CTAs per cluster along M (two: neighbouring row tiles)
+  bool pair;  // cm == 2: one cta_group::2 MMA per pair, each CTA holding half the Y tile
+              // (otherwise each CTA multiplies alone and the Y tile is multicast)
 };
 
 // Largest dynamic shared memory a CTA may request (227 KiB on sm_100-class parts).

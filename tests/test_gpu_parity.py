@@ -146,22 +146,26 @@ def test_stream_k_split(agmm, streamk, monkeypatch):
         assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
 
 
-@pytest.mark.parametrize("case", [(3, 200, 1024, 512, False), (5, 300, 512, 256, True), (8, 130, 256, 640, True)])
-def test_cluster_multicast_matches_single_cta(agmm, case, monkeypatch):
-    # Pairs of CTAs share each Y tile through TMA multicast; without stream-K
-    # the arithmetic is unchanged, so the output is bitwise equal to one CTA
-    # per cluster.  Odd row-tile counts exercise the idle second CTA.
+@pytest.mark.parametrize("case", [(3, 200, 1024, 512, False), (5, 300, 512, 256, True), (8, 130, 256, 640, True),
+                                  (4, 256, 768, 768, False)])
+def test_cluster_variants(agmm, case, monkeypatch):
+    # Row tiles in clusters of two: either one cta_group::2 MMA per pair (each
+    # CTA holds half the Y tile) or one MMA per CTA with the Y tile multicast.
+    # Without stream-K the multicast variant is bitwise equal to one CTA per
+    # cluster; every variant meets the oracle tolerance.  Odd row-tile counts
+    # exercise an idle second CTA.
     P, m, k, n, rt = case
     xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=6)
     ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
     monkeypatch.setenv("AGMM_STREAMK", "0")
     outs = {}
-    for cm in ("1", "2"):
+    for name, cm, pair in (("single", "1", "0"), ("multicast", "2", "0"), ("pair", "2", "1")):
         monkeypatch.setenv("AGMM_CM", cm)
+        monkeypatch.setenv("AGMM_PAIR", pair)
         o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=P - 1)
-        check(o, ref32, f"cm={cm} {plan.info()}")
-        outs[cm] = o
-    assert torch.equal(outs["1"].view(torch.int16), outs["2"].view(torch.int16))
+        check(o, ref32, f"{name} {plan.info()}")
+        outs[name] = o
+    assert torch.equal(outs["single"].view(torch.int16), outs["multicast"].view(torch.int16))
 
 
 @pytest.mark.parametrize("mode", ["half", "whole"])
