@@ -48,7 +48,7 @@ class PlanInfo(ctypes.Structure):
         ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int),
         ("stages", ctypes.c_int), ("splits", ctypes.c_int), ("num_tiles", ctypes.c_int),
         ("num_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("num_sms", ctypes.c_int),
-        ("smem_bytes", ctypes.c_size_t),
+        ("smem_bytes", ctypes.c_size_t), ("row_groups", ctypes.c_int),
     ]
 
 

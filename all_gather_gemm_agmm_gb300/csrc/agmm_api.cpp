@@ -115,6 +115,9 @@ struct agmm_plan_s {
   int cluster_x = 1;
   int dp_tiles = 0, sk_tiles = 0;
   int max_clusters = 0;  // co-resident clusters (rows path)
+  bool swap_dsmem = false;  // swap path: k-split partials through DSMEM
+  int row_groups = 1;       // swap path: row groups of the gathered rows (grid z)
+  int group_chunks = 0;     // swap path: ring chunks per row group
   size_t tail_bytes = 0;  // workspace bytes for tail counters and partials
   // descriptor cache: tensor maps depend only on the X and Y pointers
   bool cache_valid = false;
@@ -184,21 +187,52 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->box_rows = best_bh;
     pl->whole_shards = best_whole;
     pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, best_bh, best_whole));
-    pl->mma_n = (int)((best_pad + 31) / 32 * 32);
     pl->num_n_tiles = (int)(pl->n / kTileM);
     pl->num_m_tiles = 1;
     pl->num_tiles = pl->num_n_tiles;
+    // Row groups: the chunks may be divided into G groups (blockIdx.z), each
+    // its own MMA N.  More groups re-read Y (once per group) and each CTA
+    // reads fewer X rows per k block; they leave more CTAs per n tile, so k
+    // needs fewer splits, and the split-K partials (splits x rows x n floats,
+    // written and read back) shrink.  Per-CTA cost model, in bytes moved
+    // per SM: k blocks x (Y box + X rows) + 4.4 x the partial's bytes (a
+    // partial is written and read back at about half the load rate).
+    const int max_splits = std::min(16, pl->num_k_blocks);
+    const int env_groups = env_int("AGMM_ROWGROUPS", 0);
+    const int env_splits = env_int("AGMM_SPLITK", 0);
+    int best_g = 1, best_s = 1;
+    double best_model = -1.0;
+    for (int G = 1; G <= pl->total_chunks; G *= 2) {
+      if (env_groups > 0 && G != env_groups) continue;
+      const int cpg = (pl->total_chunks + G - 1) / G;
+      if ((G - 1) * cpg >= pl->total_chunks) continue;  // the last group would be empty
+      const int gcols = cpg * pl->box_rows;
+      int S = pl->num_sms / (pl->num_n_tiles * G);
+      S = std::max(1, std::min(S, max_splits));
+      if (env_splits > 0) S = std::max(1, std::min(env_splits, max_splits));
+      const int kb = (pl->num_k_blocks + S - 1) / S;
+      const int mn = (gcols + 31) / 32 * 32;
+      const double model = (double)kb * (kASlotBytes + 128.0 * mn) + (S > 1 ? 4.4 * 512.0 * gcols : 0.0);
+      if (best_model < 0 || model < best_model * 0.97) {
+        best_model = model;
+        best_g = G;
+        best_s = S;
+      }
+      if (env_groups == 0 && G >= 8) break;
+    }
+    pl->row_groups = best_g;
+    pl->group_chunks = (pl->total_chunks + best_g - 1) / best_g;
+    pl->mma_n = (pl->group_chunks * pl->box_rows + 31) / 32 * 32;
     pl->b_slot_bytes = (uint32_t)pl->mma_n * 128u;
     const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
     pl->stages = (int)std::min<int64_t>(kMaxStages, budget / stage_bytes);
     pl->stages = std::min(pl->stages, std::max(2, env_int("AGMM_STAGES", kMaxStages)));
-    // Upper bound on the k splits (cluster size); plan_impl lowers it until
-    // one wave of clusters covers every n tile.
-    int splits = pl->num_sms / pl->num_n_tiles;
-    splits = std::max(1, std::min(splits, std::min(16, pl->num_k_blocks)));
-    const int env_splits = env_int("AGMM_SPLITK", 0);
-    if (env_splits > 0) splits = std::max(1, std::min(env_splits, std::min(16, pl->num_k_blocks)));
-    pl->splits = splits;
+    // The k splits (cluster size); plan_impl lowers them until one wave of
+    // clusters covers every (n tile, row group).
+    pl->splits = best_s;
+    // k-split partials go through device memory (L2) unless AGMM_SWAP_DSMEM=1
+    // routes them through distributed shared memory.
+    pl->swap_dsmem = env_int("AGMM_SWAP_DSMEM", 0) != 0;
     pl->tmem_cols = pow2_ceil(std::max(32, pl->mma_n));
     pl->group_m = 1;
   } else {
@@ -307,9 +341,11 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       // splits x cpo slots of 128 floats (cpo = owner columns, 16-aligned).
       const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
       const int64_t budget = (int64_t)kMaxDynSmem - 1024 - kCtlBytes;
-      const int64_t groups = (pl->total_chunks * (int64_t)pl->box_rows + 15) / 16;
+      const int64_t groups = (pl->group_chunks * (int64_t)pl->box_rows + 15) / 16;
       const int64_t cpo = (groups + pl->splits - 1) / pl->splits * 16;
-      const int64_t recv = (int64_t)pl->splits * cpo * kTileM * 4;
+      // With device-memory partials only the one-split local route uses it.
+      const bool via_smem = pl->splits == 1 || pl->swap_dsmem;
+      const int64_t recv = via_smem ? (int64_t)pl->splits * cpo * kTileM * 4 : 0;
       while ((int64_t)pl->stages * stage_bytes < recv && (int64_t)(pl->stages + 1) * stage_bytes <= budget &&
              pl->stages < kMaxStages)
         ++pl->stages;
@@ -339,7 +375,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       break;
     }
     if (pl->splits == 1) active *= pl->num_sms;  // CTAs per SM -> CTAs per device
-    const int needed = pl->key.path == kPathSwap ? pl->num_n_tiles : 1;
+    const int needed = pl->key.path == kPathSwap ? pl->num_n_tiles * pl->row_groups : 1;
     if (active >= needed || (pl->splits == 1 && active > 0)) break;
     if (pl->splits <= 1) {
       delete pl;
@@ -348,8 +384,12 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
     --pl->splits;
   }
   if (pl->key.path == kPathSwap) {
-    pl->grid = dim3((unsigned)pl->splits, (unsigned)pl->num_n_tiles, 1);
+    pl->grid = dim3((unsigned)pl->splits, (unsigned)pl->num_n_tiles, (unsigned)pl->row_groups);
     pl->cluster_x = pl->splits;
+    if (pl->splits > 1 && !pl->swap_dsmem) {
+      const int64_t groups = (pl->group_chunks * (int64_t)pl->box_rows + 15) / 16;
+      pl->tail_bytes = (size_t)pl->num_n_tiles * pl->row_groups * pl->splits * groups * 4 * kTileM * 16;
+    }
   } else {
     // Persistent clusters, one CTA per SM.  Whole waves of cluster tiles are
     // dealt round-robin; when the tile count is not a multiple of the
@@ -388,6 +428,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.box_shift = 0;
   while ((1 << kp.box_shift) < pl->box_rows) ++kp.box_shift;
   kp.total_chunks = pl->total_chunks;
+  kp.group_chunks = pl->key.path == kPathSwap ? pl->group_chunks : pl->total_chunks;
   kp.num_m_tiles = pl->num_m_tiles;
   kp.num_mc_tiles = pl->num_mc_tiles;
   kp.num_n_tiles = pl->num_n_tiles;
@@ -401,6 +442,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.b_slot_bytes = pl->b_slot_bytes;
   kp.wait_limit_ns = (uint64_t)std::max(1, env_int("AGMM_WAIT_LIMIT_MS", 2000)) * 1000000ull;
   kp.test_drop_first_arrive = env_int("AGMM_TEST_DROP_ARRIVE", 0) != 0;
+  kp.pdl = env_int("AGMM_PDL", 1) != 0;
   kp.dp_tiles = pl->dp_tiles;
   if (with_sub && P > 1) {
     st = plan_impl(1, pl->M(), k, n, dtype, rhs_t, false, &pl->sub);
@@ -465,6 +507,7 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
   kp.out = o;
   kp.status = static_cast<int*>(status);
   kp.my_id = my_id;
+  kp.swap_partials = (pl->key.path == kPathSwap && pl->tail_bytes > 0) ? static_cast<float*>(tail_ws) : nullptr;
   if (pl->sk_tiles > 0) {
     kp.sk_flags = static_cast<int*>(tail_ws);
     kp.sk_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(tail_ws) +
@@ -663,6 +706,7 @@ agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info) {
   info->group_m = plan->group_m;
   info->num_sms = plan->num_sms;
   info->smem_bytes = plan->smem_bytes;
+  info->row_groups = plan->key.path == kPathSwap ? plan->row_groups : 1;
   return AGMM_OK;
 }
 

@@ -20,8 +20,9 @@
 //   swap path  (the whole gathered LHS fits in one MMA N <= 256) MMA M = 128
 //              columns of n, MMA N = every gathered row; k is split across the
 //              CTAs of a thread-block cluster and the float32 partials are
-//              summed in a fixed rank order through distributed shared memory,
-//              so Y is read from device memory exactly once.
+//              summed in a fixed rank order (through an L2-resident
+//              workspace, or distributed shared memory), so Y is read from
+//              device memory once per row group of the gathered rows.
 //
 // Every mbarrier wait is bounded (KernelParams::wait_limit_ns).  A wait that
 // runs out raises a shared abort flag and records AGMM_ERR_TIMEOUT in the
@@ -56,10 +57,6 @@ __device__ __forceinline__ uint32_t bar_drain(uint32_t ctl) {
 // (1 arrival) and the contributors' "partial stored" (128 arrivals).
 __device__ __forceinline__ uint32_t bar_owner_go(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 5); }
 __device__ __forceinline__ uint32_t bar_published(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 6); }
-// CTA pairs: the follower's "stage s landed" forwarded to the leader.
-__device__ __forceinline__ uint32_t bar_peer_full(uint32_t ctl, int s) {
-  return ctl + 8u * (2 * kMaxStages + 7 + s);
-}
 constexpr int kAbortOffset = 8 * (3 * kMaxStages + 7);  // int
 constexpr int kTmemOffset = kAbortOffset + 16;          // uint32
 constexpr int kChunkTabOffset = 512;                    // int4[kMaxSwapChunks]: shard, src_row, valid, out_row
@@ -97,7 +94,7 @@ __device__ __forceinline__ int wait_phase(uint32_t bar, uint32_t parity, volatil
 
 // Trace slot written by one thread (not lane 0 of each warp).
 __device__ __forceinline__ void trace_value(const KernelParams& p, int slot, uint64_t v) {
-  if (p.trace != nullptr) p.trace[(size_t)(blockIdx.x + gridDim.x * blockIdx.y) * kTraceSlots + slot] = v;
+  if (p.trace != nullptr) p.trace[(size_t)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)) * kTraceSlots + slot] = v;
 }
 
 // Bounded wait that ignores the abort flag: used to drain work in flight.
@@ -125,7 +122,7 @@ __device__ __noinline__ void record_failure(const KernelParams& p, volatile int*
 // Opt-in device trace: %globaltimer stamps per CTA (16 slots of u64).
 __device__ __forceinline__ void trace(const KernelParams& p, int slot) {
   if (p.trace != nullptr && (threadIdx.x & 31) == 0) {
-    const uint32_t cta = blockIdx.x + gridDim.x * blockIdx.y;
+    const uint32_t cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
     p.trace[(size_t)cta * kTraceSlots + slot] = ptx::globaltimer_ns();
   }
 }
@@ -289,13 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   const uint64_t limit = p.wait_limit_ns;
 
   if (warp == 0) trace(p, 0);
+  // The next kernel in the stream may start its prologue on free SMs; it waits
+  // (griddepcontrol.wait) for this grid to finish before touching memory.
+  if (threadIdx.x == 0) ptx::griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       // a pair: both producers count their bytes on the leader's barrier
       ptx::mbar_init(bar_full(ctl, s), kPair ? 2 : 1);
       // every cluster CTA's MMA frees the stage (a pair: the leader's MMA alone)
       ptx::mbar_init(bar_empty(ctl, s), kPair ? 1 : kCM);
-      ptx::mbar_init(bar_peer_full(ctl, s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_acc_full(ctl, a), 1);
@@ -313,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     ptx::prefetch_tensormap(&p.ymap);
   }
   if constexpr (kPath == kPathSwap) {
-    // The ring-ordered chunk table, computed once per CTA (the swap path keeps
-    // every chunk of the gathered LHS in one MMA N).
+    // The ring-ordered chunk table, computed once per CTA (each row group of
+    // the swap path keeps its chunks of the gathered LHS in one MMA N).
     if (warp == 2 && lane < p.total_chunks) {
       const RingChunk ch = ring_chunk(geom, lane);
       chunk_tab[lane] = make_int4(ch.shard, (int)ch.src_row, ch.valid, (int)ch.out_row);
@@ -331,12 +330,21 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (kCM > 1) {
+    // Peers multicast into this CTA's shared memory and signal its barriers:
+    // none may do so before every CTA of the cluster has initialised them.
+    ptx::cluster_arrive_relaxed();
+    ptx::cluster_wait();
+  }
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above touched only shared memory, tensor memory and the
+  // parameter block; from here on the previous grid's writes must be visible.
+  ptx::griddep_wait();
   if (warp == 0) {
     trace(p, 1);
     if (p.trace != nullptr && lane == 0) {
-      const uint32_t cta = blockIdx.x + gridDim.x * blockIdx.y;
+      const uint32_t cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
       p.trace[(size_t)cta * kTraceSlots + 12] = ptx::smid();
       p.trace[(size_t)cta * kTraceSlots + 13] = ptx::cluster_ctarank();
     }
@@ -346,6 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   // Swap path: n tile blockIdx.y, k split blockIdx.x (= rank in the cluster).
   const int swap_nt = (kPath == kPathSwap) ? (int)blockIdx.y : 0;
   const int split = (kPath == kPathSwap) ? (int)blockIdx.x : 0;
+  // Swap path row group blockIdx.z: ring chunks [swap_c0, swap_c0 + swap_nch).
+  const int swap_c0 = (kPath == kPathSwap) ? (int)blockIdx.z * p.group_chunks : 0;
+  const int swap_nch = (kPath == kPathSwap) ? min(p.group_chunks, p.total_chunks - swap_c0) : 0;
+  const int swap_cl = (kPath == kPathSwap) ? (int)(blockIdx.z * gridDim.y + blockIdx.y) : 0;  // cluster index
   const int kb_begin = (kPath == kPathSwap) ? (int)((int64_t)split * p.num_k_blocks / p.splits) : 0;
   const int kb_end =
       (kPath == kPathSwap) ? (int)((int64_t)(split + 1) * p.num_k_blocks / p.splits) : p.num_k_blocks;
@@ -397,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         } else {
           if (!swap_pending) break;
           swap_pending = false;
-          bytes = (uint32_t)kASlotBytes + (uint32_t)p.total_chunks * p.box_rows * 128u;
+          bytes = (uint32_t)kASlotBytes + (uint32_t)swap_nch * p.box_rows * 128u;
         }
         for (int kb = kb0; kb < kb1; ++kb) {
           const int res = wait_phase(bar_empty(ctl, stage), phase ^ 1u, abort_flag, limit, wait_acc);
@@ -483,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
                   ptx::tma_load_2d(a_dst + (uint32_t)a * 8192u, &p.ymap, full, nt * kTileM + a * 64, k0);
               }
               const uint32_t chunk_bytes = (uint32_t)p.box_rows * 128u;
-              for (int c = 0; c < p.total_chunks; ++c) {
-                const int4 e = chunk_tab[c];
+              for (int c = 0; c < swap_nch; ++c) {
+                const int4 e = chunk_tab[swap_c0 + c];
                 ptx::tma_load_2d(b_dst + (uint32_t)c * chunk_bytes, &p.xmap[e.x], full, k0, e.y);
               }
             }
@@ -772,23 +784,57 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   }
 
   if constexpr (kPath == kPathSwap) {
-    // Reduction of the k splits.  Owner ranks hold groups of 16 gathered-row
-    // slots: rank o owns slots [o*cpo, (o+1)*cpo), cpo a multiple of 16.  In
-    // the owner's shared memory recv[r][lq][lane][4] holds rank r's partial of
-    // its slots 4*lq..4*lq+3 for one TMEM lane (one n column).  Ranks push their
-    // partials with 16-byte remote stores once every CTA's pipeline memory is
-    // idle (barrier 1); after barrier 2 each owner sums recv[0..splits-1] in
-    // rank order, so the result does not depend on timing.  With one split the
-    // CTA is its own owner.
-    const int ncols = p.total_chunks * p.box_rows;
+    // Reduction of the k splits of this CTA's (n tile, row group).  The
+    // accumulator holds 128 n columns (TMEM lanes) x ncols gathered-row slots
+    // (TMEM columns): chunks c0.. of the ring-ordered chunk table, box_rows
+    // slots each.  With one split the CTA is its own owner.
+    const int ncols = swap_nch * p.box_rows;
     const int S = p.splits;
     const int groups = (ncols + 15) >> 4;
+    // Slot size of the device-memory mode: the widest row group's columns.
+    const int slot_groups = (p.group_chunks * p.box_rows + 15) >> 4;
+    const size_t slot_quads = (size_t)slot_groups * 4;
+    // Device-memory mode: each rank stores its partial to its own slot
+    // [quad][128 lanes][4 floats] in an L2-resident workspace with coalesced
+    // 16-byte stores; barrier 2 (release/acquire at cluster scope) orders them
+    // before the owners' loads.  Owner o sums quads [o*Q/S, (o+1)*Q/S) over
+    // every rank, in rank order.
+    // Shared-memory mode: owner o holds 16-slot groups [o*cpo, (o+1)*cpo) and
+    // recv[r][lq][lane][4] in its shared memory receives rank r's partial of
+    // slots 4*lq..4*lq+3; ranks push with 16-byte remote stores once every
+    // CTA's pipeline memory is idle (barrier 1).
+    const bool global_mode = S > 1 && p.swap_partials != nullptr;
     const int cpo = ((groups + S - 1) / S) * 16;
     const uint32_t quad_bytes = (uint32_t)kTileM * 16u;  // one [lane][4] block
+    float4* gslot = global_mode ? reinterpret_cast<float4*>(p.swap_partials) +
+                                      ((size_t)swap_cl * S) * slot_quads * kTileM
+                                : nullptr;
     __syncwarp();
-    if (S > 1) ptx::cluster_sync_all();  // 1: all CTAs have drained their main loop
+    if (S > 1 && !global_mode) ptx::cluster_sync_all();  // 1: all CTAs have drained their main loop
     trace(p, 8);
-    if (warp >= 2) {
+    if (warp >= 2 && global_mode) {
+      const int tl = (warp & 3) * 32 + lane;
+      float4* mine = gslot + (size_t)split * slot_quads * kTileM + tl;
+      const uint32_t tbase = lane_base_of(tmem_base, warp);
+#pragma unroll 1
+      for (int g = 0; g < groups; g += 2) {
+        uint32_t v[2][16];
+        ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 16), v[0]);
+        if (g + 1 < groups) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)((g + 1) * 16), v[1]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (g + h < groups) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              mine[((size_t)(g + h) * 4 + q4) * kTileM] =
+                  make_float4(__uint_as_float(v[h][4 * q4]), __uint_as_float(v[h][4 * q4 + 1]),
+                              __uint_as_float(v[h][4 * q4 + 2]), __uint_as_float(v[h][4 * q4 + 3]));
+          }
+        }
+      }
+      ptx::tc_fence_before();
+    } else if (warp >= 2) {
       const uint32_t lane_off = (uint32_t)(((warp & 3) * 32 + lane) * 16);
       const uint32_t my_slot0 = base + (uint32_t)(split * (cpo >> 2)) * quad_bytes + lane_off;
       const uint32_t tbase = lane_base_of(tmem_base, warp);
@@ -835,7 +881,58 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     __syncwarp();
     if (S > 1) ptx::cluster_sync_all(); else __syncthreads();  // 2: partials delivered
     trace(p, 9);
-    if (warp >= 2 && !*abort_flag) {
+    if (global_mode) {
+      if (!*abort_flag) {
+        // The (quad, column) items are spread over all warps, two per round,
+        // so each thread has 2 * splits independent loads in flight.
+        const int Q = ncols >> 2;
+        const int q0 = (int)(((int64_t)split * Q) / S);
+        const int q1 = (int)(((int64_t)(split + 1) * Q) / S);
+        const int items = (q1 - q0) * kTileM;
+#pragma unroll 1
+        for (int i = threadIdx.x; i < items; i += 2 * kThreads) {
+          float4 part[2][kMaxSplits];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int it = i + h * kThreads;
+            if (it < items) {
+              const size_t q = (size_t)(q0 + (it >> 7));
+              const int t = it & (kTileM - 1);
+#pragma unroll
+              for (int rk = 0; rk < kMaxSplits; ++rk)
+                if (rk < S) part[h][rk] = __ldcg(gslot + ((size_t)rk * slot_quads + q) * kTileM + t);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int it = i + h * kThreads;
+            if (it < items) {
+              const int q = q0 + (it >> 7);
+              const int t = it & (kTileM - 1);
+              float4 sum = part[h][0];
+#pragma unroll
+              for (int rk = 1; rk < kMaxSplits; ++rk) {
+                if (rk < S) {
+                  sum.x += part[h][rk].x;
+                  sum.y += part[h][rk].y;
+                  sum.z += part[h][rk].z;
+                  sum.w += part[h][rk].w;
+                }
+              }
+              const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+              const int64_t ncol = (int64_t)swap_nt * kTileM + t;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int cj = q * 4 + j;
+                const int4 e = chunk_tab[swap_c0 + (cj >> p.box_shift)];
+                const int r = cj & (p.box_rows - 1);
+                if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j]);
+              }
+            }
+          }
+        }
+      }
+    } else if (warp >= 2 && !*abort_flag) {
       // Thread t sums lane t (n column swap_nt*128 + t) of four slots at a time.
       const int t = threadIdx.x - 64;
       const int c0 = split * cpo;
@@ -865,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         for (int j = 0; j < 4; ++j) {
           const int cj = c + j;
           if (cj < c1) {
-            const int4 e = chunk_tab[cj >> p.box_shift];
+            const int4 e = chunk_tab[swap_c0 + (cj >> p.box_shift)];
             const int r = cj & (p.box_rows - 1);
             if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j]);
           }
@@ -986,7 +1083,7 @@ cudaError_t launch_agmm_kernel(const KernelKey& key, const KernelParams& p, dim3
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   unsigned na = 0;
   if (cluster_x > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
@@ -998,6 +1095,13 @@ cudaError_t launch_agmm_kernel(const KernelKey& key, const KernelParams& p, dim3
   if (cooperative) {
     attr[na].id = cudaLaunchAttributeCooperative;
     attr[na].val.cooperative = 1;
+    ++na;
+  } else if (p.pdl) {
+    // Programmatic dependent launch: this grid's prologue may overlap the
+    // previous kernel's tail; the kernel waits (griddepcontrol.wait) before
+    // its first global-memory access.
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
   cfg.attrs = na ? attr : nullptr;

@@ -26,7 +26,7 @@ enum Path : int { kPathRows = 0, kPathSwap = 1 };
 //   [0] first error code (0 = none), [1] role that gave up, [2] stage, [3] tile.
 enum StatusRole : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
 
-struct __align__(64) KernelParams {
+struct __align__(128) KernelParams {
   CUtensorMap xmap[kMaxShards];  // shard r: [m_pd, k] bf16, box {64, box_rows}, 128B swizzle
   CUtensorMap ymap;              // Y: K-major box {64, rows} or MN-major box {64, 64}
   void* out;                     // O [P*m_pd, n], bf16 or f32
@@ -65,6 +65,12 @@ struct __align__(64) KernelParams {
   int sk_min_units;              // unused on the device; planner bookkeeping
   int* sk_flags;                 // [sk tiles][cluster rank] arrival counters (zero between runs)
   float* sk_partials;            // [clusters][cluster rank][BN/32][8][128][4]
+  // Swap path with k splits: float32 partials in device memory
+  // [row group][n tile][split][quad][128 lanes][4] (null: the partials go
+  // through distributed shared memory instead).
+  float* swap_partials;
+  int group_chunks;  // swap path: ring chunks per row group (blockIdx.z)
+  int pdl;  // launched with programmatic stream serialization (host side only)
 };
 
 struct GatherParams {

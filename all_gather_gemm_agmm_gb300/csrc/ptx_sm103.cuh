@@ -298,6 +298,23 @@ __device__ __forceinline__ void cluster_sync_all() {
                    : "memory");
 }
 
+// Split cluster barrier: arrive (relaxed: pairs with fence.mbarrier_init) and
+// wait (acquire).  Every thread of every CTA in the cluster takes part.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue; wait until every prerequisite grid has completed and its memory
+// operations are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Address of the same shared-memory offset in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;

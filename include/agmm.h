@@ -81,6 +81,7 @@ typedef struct {
   int group_m;       /* row tiles per raster group                               */
   int num_sms;       /* SMs of the planned device                                */
   size_t smem_bytes; /* dynamic shared memory per CTA                            */
+  int row_groups;    /* swapped tiles: groups of chunks, one MMA N each (else 1) */
 } agmm_plan_info_t;
 
 /*

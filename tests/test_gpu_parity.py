@@ -183,3 +183,35 @@ def test_chunking_modes(agmm, case, mode, monkeypatch):
     o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=P // 2)
     assert plan.info()["whole_shards"] == (mode == "whole")
     check(o, ref32, f"{mode} {plan.info()}")
+
+
+@pytest.mark.parametrize("case", [(4, 64, 1024, 512, True), (5, 40, 512, 256, False), (3, 13, 768, 384, True),
+                                  (8, 32, 512, 256, False)],
+                         ids=lambda c: "P{}_m{}_k{}".format(c[0], c[1], c[2]))
+def test_swap_row_groups(agmm, case, monkeypatch):
+    # The swapped path may divide the ring-ordered chunks into row groups,
+    # each its own MMA N.  With the k splits fixed, every output element is
+    # reduced in the same order whatever the grouping, so the groupings agree
+    # bitwise; both reduction routes (device memory, distributed shared
+    # memory) meet the oracle tolerance.  Odd chunk counts leave a short last
+    # group.
+    P, m, k, n, rt = case
+    xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=9)
+    ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+    monkeypatch.setenv("AGMM_PATH", "1")
+    monkeypatch.setenv("AGMM_SPLITK", "4")
+    outs = {}
+    for dsmem in ("0", "1"):
+        monkeypatch.setenv("AGMM_SWAP_DSMEM", dsmem)
+        for groups in ("1", "2", "4"):
+            monkeypatch.setenv("AGMM_ROWGROUPS", groups)
+            o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=P - 1)
+            info = plan.info()
+            assert info["path"] == 1
+            if info["row_groups"] != int(groups):
+                continue  # that many groups would leave one empty
+            check(o, ref32, f"groups={groups} dsmem={dsmem} {info}")
+            outs[(dsmem, groups)] = o
+    base = outs[("0", "1")]
+    for key, o in outs.items():
+        assert torch.equal(base.view(torch.int16), o.view(torch.int16)), key
