@@ -117,6 +117,7 @@ struct agmm_plan_s {
   int max_clusters = 0;  // co-resident clusters (rows path)
   bool swap_dsmem = false;  // swap path: k-split partials through DSMEM
   int row_groups = 1;       // swap path: row groups of the gathered rows (grid z)
+  int clock_khz = 2100000;  // peak SM clock of the planned device
   int group_chunks = 0;     // swap path: ring chunks per row group
   size_t tail_bytes = 0;  // workspace bytes for tail counters and partials
   // descriptor cache: tensor maps depend only on the X and Y pointers
@@ -311,6 +312,11 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return fail_cuda(e, "cudaDeviceGetAttribute");
+  int clock_khz = 0;
+  if (cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, dev) != cudaSuccess || clock_khz <= 0) {
+    (void)cudaGetLastError();
+    clock_khz = 2100000;  // above the part's 2.07 GHz peak
+  }
   if (major != 10 || minor != 3)
     return fail(AGMM_ERR_UNSUPPORTED, "this library is built for sm_103a only; device is sm_" +
                                           std::to_string(major) + std::to_string(minor));
@@ -324,6 +330,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   pl->rhs_t = rhs_t;
   pl->device = dev;
   pl->num_sms = sms;
+  pl->clock_khz = clock_khz;
   pl->key.y_kmajor = rhs_t != 0;
   pl->key.out_f32 = dtype == AGMM_BF16_F32OUT;
   pl->out_elem = pl->key.out_f32 ? 4 : 2;
@@ -440,7 +447,9 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.tmem_cols = pl->tmem_cols;
   kp.splits = pl->splits;
   kp.b_slot_bytes = pl->b_slot_bytes;
-  kp.wait_limit_ns = (uint64_t)std::max(1, env_int("AGMM_WAIT_LIMIT_MS", 2000)) * 1000000ull;
+  // The kernels bound their waits in SM cycles: a limit converted at the
+  // peak clock (kHz = cycles per millisecond) lasts at least that long.
+  kp.wait_limit_cycles = (uint64_t)std::max(1, env_int("AGMM_WAIT_LIMIT_MS", 2000)) * (uint64_t)pl->clock_khz;
   kp.test_drop_first_arrive = env_int("AGMM_TEST_DROP_ARRIVE", 0) != 0;
   kp.pdl = env_int("AGMM_PDL", 1) != 0;
   kp.dp_tiles = pl->dp_tiles;

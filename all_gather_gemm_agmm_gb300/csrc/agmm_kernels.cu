@@ -24,7 +24,7 @@
 //              workspace, or distributed shared memory), so Y is read from
 //              device memory once per row group of the gathered rows.
 //
-// Every mbarrier wait is bounded (KernelParams::wait_limit_ns).  A wait that
+// Every mbarrier wait is bounded (KernelParams::wait_limit_cycles).  A wait that
 // runs out raises a shared abort flag and records AGMM_ERR_TIMEOUT in the
 // status words; all roles then leave their loops, wait (bounded) for their own
 // TMA and MMA work in flight, and the CTA frees its tensor memory and returns.
@@ -75,19 +75,21 @@ __device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
     return ptx::mbar_try_wait(bar, parity);
 }
 
+// The bound is in SM clock cycles (the host converts the time limit at the
+// device's peak clock, so a wait lasts at least that long).
 template <bool kClusterScope = false>
 __device__ __forceinline__ int wait_phase(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns, uint64_t* waited = nullptr) {
+                                          uint64_t limit_cycles, uint64_t* waited = nullptr) {
   if (try_wait_scoped<kClusterScope>(bar, parity)) return kWaitOk;
-  const uint64_t t0 = ptx::globaltimer_ns();
+  const uint64_t t0 = ptx::clock_cycles();
   for (uint32_t it = 1;; ++it) {
     if (try_wait_scoped<kClusterScope>(bar, parity)) {
-      if (waited) *waited += ptx::globaltimer_ns() - t0;
+      if (waited) *waited += ptx::clock_cycles() - t0;
       return kWaitOk;
     }
     if ((it & 15u) == 0u) {
       if (*abort) return kWaitAborted;
-      if (ptx::globaltimer_ns() - t0 > limit_ns) return kWaitTimeout;
+      if (ptx::clock_cycles() - t0 > limit_cycles) return kWaitTimeout;
     }
   }
 }
@@ -98,12 +100,12 @@ __device__ __forceinline__ void trace_value(const KernelParams& p, int slot, uin
 }
 
 // Bounded wait that ignores the abort flag: used to drain work in flight.
-__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_cycles) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
+  const uint64_t t0 = ptx::clock_cycles();
   for (uint32_t it = 1;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0u && ptx::globaltimer_ns() - t0 > limit_ns) return false;
+    if ((it & 15u) == 0u && ptx::clock_cycles() - t0 > limit_cycles) return false;
   }
 }
 
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const RingGeom geom = make_ring_geom(p.P, p.m_pd, p.my_id, p.box_rows, p.whole_shards);
-  const uint64_t limit = p.wait_limit_ns;
+  const uint64_t limit = p.wait_limit_cycles;
 
   if (warp == 0) trace(p, 0);
   // The next kernel in the stream may start its prologue on free SMs; it waits
@@ -667,10 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           if (threadIdx.x == 64) {
             int wres = kWaitOk;
             const int* flag = p.sk_flags + (size_t)(sg.tile - p.dp_tiles) * kCM + crank;
-            const uint64_t t0 = ptx::globaltimer_ns();
+            const uint64_t t0 = ptx::clock_cycles();
             while (ld_acquire_gpu(flag) < ncontrib) {
               if (*abort_flag) { wres = kWaitAborted; break; }
-              if (ptx::globaltimer_ns() - t0 > limit) { wres = kWaitTimeout; break; }
+              if (ptx::clock_cycles() - t0 > limit) { wres = kWaitTimeout; break; }
               __nanosleep(32);
             }
             if (wres == kWaitOk) {

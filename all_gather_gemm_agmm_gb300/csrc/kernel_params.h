@@ -15,7 +15,7 @@ constexpr int kTileM = 128;         // MMA M (one CTA, 128 TMEM lanes)
 constexpr int kTileK = 64;          // k per stage: one 128-byte swizzle row of bf16
 constexpr int kASlotBytes = kTileM * kTileK * 2;  // 16 KiB
 constexpr int kStatusBytes = 256;   // status words at the start of the workspace
-constexpr int kTraceSlots = 16;     // u64 %globaltimer stamps per CTA in the optional trace
+constexpr int kTraceSlots = 16;     // u64 slots per CTA in the optional trace
 constexpr int kCtlBytes = 1024;     // per-CTA control block: barriers, flags, swap-path chunk table
 constexpr int kMaxSwapChunks = 32;  // swap path: at most 256 rows in chunks of >= 8 rows
 constexpr int kMaxSplits = 16;      // swap path: largest cluster (non-portable size 16)
@@ -50,7 +50,7 @@ struct __align__(128) KernelParams {
   int tmem_cols;                 // TMEM columns allocated (power of two >= 32)
   int splits;                    // swap path: k splits = cluster size
   uint32_t b_slot_bytes;         // bytes of one B-operand stage slot (multiple of 1024)
-  uint64_t wait_limit_ns;        // bound on every mbarrier wait
+  uint64_t wait_limit_cycles;    // bound on every wait, in SM clock cycles
   int test_drop_first_arrive;    // test hook: producer skips its first arrival
   uint64_t* trace;               // optional [CTAs][kTraceSlots] timestamps (null: off)
   // Rows path work (hybrid stream-K).  Cluster tiles [0, dp_tiles) are dealt

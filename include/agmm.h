@@ -190,12 +190,13 @@ agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream)
  * Optional device trace: after agmm_set_trace(plan, buf, bytes) every
  * agmm_run of this plan writes, per CTA, 16 unsigned 64-bit slots to the
  * device buffer `buf` (agmm_trace_bytes(plan) bytes, 8-byte aligned): %globaltimer
- * nanoseconds at kernel entry (0), after set-up (1), first and last TMA issue
+ * nanoseconds (the stamps themselves cost a few hundred cycles each) at
+ * kernel entry (0), after set-up (1), first and last TMA issue
  * (2, 3), first operand arrival at the MMA thread (4), last MMA commit (5),
  * first accumulator seen by the epilogue (6), rows-path epilogue done (7),
  * swap-path reduction barriers (8, 9), reduction stored (10), exit (11), plus
  * the SM id (12) and cluster rank (13).  On the row path slots 9, 10, 14 and
- * 15 instead hold nanoseconds spent blocked: epilogue waiting for an
+ * 15 instead hold SM clock cycles spent blocked: epilogue waiting for an
  * accumulator (9), producer waiting for a free stage (10), MMA thread waiting
  * for operands (14) and for a free accumulator (15).  Pass NULL to switch it
  * off.  The buffer stays owned by the caller and must outlive the runs that
