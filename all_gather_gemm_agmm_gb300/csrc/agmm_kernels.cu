@@ -256,6 +256,66 @@ __device__ __forceinline__ void store_row4(void* out, int64_t ldo, int64_t row, 
   }
 }
 
+// Swap path, device-memory mode: owner `split` of one (n tile, row group)
+// sums quads [q0, q0 + items/128) of every rank's slot.  A quad is four
+// gathered-row slots of all 128 columns, stored [quad][128 lanes][4 floats].
+struct OwnerSlice {
+  const float4* gslot;  // rank 0's slot of this (n tile, row group)
+  size_t slot_quads;    // quads per rank's slot
+  int q0;               // first quad owned
+  int items;            // owned (quad, column) pairs
+  const int4* chunk_tab;
+  int c0;               // first chunk of the row group
+  int nt;               // n tile
+};
+
+// The (quad, column) items are spread over all warps.  Each thread issues
+// every rank's 16-byte load for kH items before summing (kH x kS loads in
+// flight, at most 24), then adds them in rank order.
+template <bool kF32, int kS>
+__device__ __forceinline__ void owner_sum_global(const KernelParams& p, const OwnerSlice& os) {
+  constexpr int kH = (24 / kS) < 1 ? 1 : ((24 / kS) > 4 ? 4 : (24 / kS));
+#pragma unroll 1
+  for (int i = threadIdx.x; i < os.items; i += kH * kThreads) {
+    float4 part[kH][kS];
+#pragma unroll
+    for (int h = 0; h < kH; ++h) {
+      const int it = i + h * kThreads;
+      if (it < os.items) {
+        const size_t q = (size_t)(os.q0 + (it >> 7));
+        const int t = it & (kTileM - 1);
+#pragma unroll
+        for (int rk = 0; rk < kS; ++rk) part[h][rk] = __ldcg(os.gslot + ((size_t)rk * os.slot_quads + q) * kTileM + t);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kH; ++h) {
+      const int it = i + h * kThreads;
+      if (it < os.items) {
+        const int q = os.q0 + (it >> 7);
+        const int t = it & (kTileM - 1);
+        float4 sum = part[h][0];
+#pragma unroll
+        for (int rk = 1; rk < kS; ++rk) {
+          sum.x += part[h][rk].x;
+          sum.y += part[h][rk].y;
+          sum.z += part[h][rk].z;
+          sum.w += part[h][rk].w;
+        }
+        const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+        const int64_t ncol = (int64_t)os.nt * kTileM + t;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int cj = q * 4 + j;
+          const int4 e = os.chunk_tab[os.c0 + (cj >> p.box_shift)];
+          const int r = cj & (p.box_rows - 1);
+          if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j]);
+        }
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // The fused kernel.  kPath: kPathRows / kPathSwap.  kYK: Y stored [n, k]
 // (K-major tiles); otherwise Y is [k, n] and its tiles are MN-major.  kF32:
@@ -885,53 +945,21 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     trace(p, 9);
     if (global_mode) {
       if (!*abort_flag) {
-        // The (quad, column) items are spread over all warps, two per round,
-        // so each thread has 2 * splits independent loads in flight.
         const int Q = ncols >> 2;
         const int q0 = (int)(((int64_t)split * Q) / S);
         const int q1 = (int)(((int64_t)(split + 1) * Q) / S);
-        const int items = (q1 - q0) * kTileM;
-#pragma unroll 1
-        for (int i = threadIdx.x; i < items; i += 2 * kThreads) {
-          float4 part[2][kMaxSplits];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int it = i + h * kThreads;
-            if (it < items) {
-              const size_t q = (size_t)(q0 + (it >> 7));
-              const int t = it & (kTileM - 1);
-#pragma unroll
-              for (int rk = 0; rk < kMaxSplits; ++rk)
-                if (rk < S) part[h][rk] = __ldcg(gslot + ((size_t)rk * slot_quads + q) * kTileM + t);
-            }
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int it = i + h * kThreads;
-            if (it < items) {
-              const int q = q0 + (it >> 7);
-              const int t = it & (kTileM - 1);
-              float4 sum = part[h][0];
-#pragma unroll
-              for (int rk = 1; rk < kMaxSplits; ++rk) {
-                if (rk < S) {
-                  sum.x += part[h][rk].x;
-                  sum.y += part[h][rk].y;
-                  sum.z += part[h][rk].z;
-                  sum.w += part[h][rk].w;
-                }
-              }
-              const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
-              const int64_t ncol = (int64_t)swap_nt * kTileM + t;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int cj = q * 4 + j;
-                const int4 e = chunk_tab[swap_c0 + (cj >> p.box_shift)];
-                const int r = cj & (p.box_rows - 1);
-                if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j]);
-              }
-            }
-          }
+        const OwnerSlice os{gslot, slot_quads, q0, (q1 - q0) * kTileM, chunk_tab, swap_c0, swap_nt};
+        switch (S) {
+#define AGMM_OWNER_CASE(N) \
+  case N:                  \
+    owner_sum_global<kF32, N>(p, os); \
+    break;
+          AGMM_OWNER_CASE(2) AGMM_OWNER_CASE(3) AGMM_OWNER_CASE(4) AGMM_OWNER_CASE(5) AGMM_OWNER_CASE(6)
+          AGMM_OWNER_CASE(7) AGMM_OWNER_CASE(8) AGMM_OWNER_CASE(9) AGMM_OWNER_CASE(10) AGMM_OWNER_CASE(11)
+          AGMM_OWNER_CASE(12) AGMM_OWNER_CASE(13) AGMM_OWNER_CASE(14) AGMM_OWNER_CASE(15) AGMM_OWNER_CASE(16)
+#undef AGMM_OWNER_CASE
+          default:
+            break;
         }
       }
     } else if (warp >= 2 && !*abort_flag) {
