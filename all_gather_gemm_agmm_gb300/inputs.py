@@ -9,8 +9,8 @@ Recipe (one reading of the workloads, stated once here):
 
 * A CPU ``torch.Generator`` seeded with ``seed`` (0 unless stated) draws, in
   this order, ``X_0 .. X_{P-1}`` (each ``[m_per_device, k]``) and then ``Y``.
-* Values are drawn in float32 and rounded to bfloat16 by PyTorch's
-  round-to-nearest-even cast.
+* Values are drawn in float32 and rounded to bfloat16 (or, for the fp16
+  variant, float16) by PyTorch's round-to-nearest-even cast.
 * ``Y`` is drawn directly in its stored layout: ``[k, n]`` when
   ``rhs_transpose`` is false, ``[n, k]`` when it is true (the flag of the
   Pallas TPU kernel's ``all_gather_matmul`` API).
@@ -84,9 +84,11 @@ for _w in SWEEP:
 
 
 def make_inputs(P: int, m_per_device: int, k: int, n: int, rhs_transpose: bool,
-                dist: str = "normal", seed: int = 0, y_std: float = 0.02
+                dist: str = "normal", seed: int = 0, y_std: float = 0.02, dtype: str = "bf16"
                 ) -> Tuple[List[torch.Tensor], torch.Tensor]:
-    """Draw the P bf16 shards and bf16 ``Y`` on the CPU (see module recipe)."""
+    """Draw the P shards and ``Y`` on the CPU (see module recipe); ``dtype``
+    "bf16" or "f16" is the type the float32 draws are rounded to."""
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     xs = []
@@ -97,13 +99,13 @@ def make_inputs(P: int, m_per_device: int, k: int, n: int, rhs_transpose: bool,
             x = torch.randn((m_per_device, k), generator=g, dtype=torch.float32)
         else:
             raise ValueError(f"unknown distribution {dist!r}")
-        xs.append(x.to(torch.bfloat16))
+        xs.append(x.to(tdt))
     yshape = (n, k) if rhs_transpose else (k, n)
     if dist == "uniform":
         y = torch.rand(yshape, generator=g, dtype=torch.float32) * 2.0 - 1.0
     else:
         y = torch.randn(yshape, generator=g, dtype=torch.float32) * y_std
-    return xs, y.to(torch.bfloat16)
+    return xs, y.to(tdt)
 
 
 def make_workload_inputs(w: Workload) -> Tuple[List[torch.Tensor], torch.Tensor]:

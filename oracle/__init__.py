@@ -5,8 +5,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 
 The arithmetic lives in ``oracle.c`` (a triple loop with explicit
 concatenation, float32 accumulation in ascending k, round-to-nearest-even cast
-to bf16); this module only builds it with gcc and marshals arrays through
-ctypes.  Every pin of the oracle is in ``tests/test_oracle.py``.
+to the 16-bit output type, bf16 or fp16); this module only builds it with gcc
+and marshals arrays through ctypes.  Every pin of the oracle is in
+``tests/test_oracle.py``.
 """
 from __future__ import annotations
 
@@ -51,6 +52,14 @@ def load(path: Optional[str] = None):
         ctypes.POINTER(ctypes.c_float), u16p, ctypes.POINTER(ctypes.c_double), ctypes.c_int,
     ]
     lib.oracle_agmm.restype = ctypes.c_int
+    lib.oracle_agmm_typed.argtypes = lib.oracle_agmm.argtypes + [ctypes.c_int]
+    lib.oracle_agmm_typed.restype = ctypes.c_int
+    lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+    lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_array_to_f16.argtypes = [ctypes.POINTER(ctypes.c_float), u16p, i64]
+    lib.oracle_f16_array_to_f32.argtypes = [u16p, ctypes.POINTER(ctypes.c_float), i64]
     lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
     lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
     lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
@@ -63,16 +72,53 @@ def load(path: Optional[str] = None):
     return lib
 
 
-def as_bf16_bits(t) -> np.ndarray:
-    """A contiguous uint16 array of bf16 bit patterns from a torch bf16 tensor
-    or a numpy uint16 array."""
+ELEM = {"bf16": 0, "f16": 1}
+
+
+def as_bits(t, dtype: str = "bf16") -> np.ndarray:
+    """A contiguous uint16 array of 16-bit patterns from a torch bf16 / fp16
+    tensor (matching ``dtype``) or a numpy uint16 array."""
     if isinstance(t, np.ndarray):
         assert t.dtype == np.uint16
         return np.ascontiguousarray(t)
     import torch  # local: the oracle itself does not depend on torch
 
-    assert t.dtype == torch.bfloat16, t.dtype
+    want = torch.bfloat16 if dtype == "bf16" else torch.float16
+    assert t.dtype == want, (t.dtype, dtype)
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def as_bf16_bits(t) -> np.ndarray:
+    """A contiguous uint16 array of bf16 bit patterns from a torch bf16 tensor
+    or a numpy uint16 array."""
+    return as_bits(t, "bf16")
+
+
+def _infer_dtype(t) -> str:
+    if isinstance(t, np.ndarray):
+        return "bf16"
+    import torch
+
+    return "f16" if t.dtype == torch.float16 else "bf16"
+
+
+def f16_bits_to_f32(bits: np.ndarray, lib=None) -> np.ndarray:
+    """fp16 bit patterns -> float32 through the oracle's own decoder."""
+    lib = lib or load()
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float32)
+    lib.oracle_f16_array_to_f32(b.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
+                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), b.size)
+    return out
+
+
+def f32_to_f16_bits(a: np.ndarray, lib=None) -> np.ndarray:
+    lib = lib or load()
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint16)
+    lib.oracle_f32_array_to_f16(a.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), a.size)
+    return out
 
 
 def bits_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -90,18 +136,23 @@ def f32_to_bf16_bits(a: np.ndarray, lib=None) -> np.ndarray:
 
 
 def agmm(xs: Sequence, y, rhs_transpose: bool, row_begin: int = 0, row_end: Optional[int] = None,
-         acc: str = "f32", nthreads: int = 0, lib=None):
+         acc: str = "f32", nthreads: int = 0, lib=None, dtype: Optional[str] = None):
     """O = concat(xs) @ (y or y.T), rows [row_begin, row_end).
 
-    ``xs``: P bf16 shards ``[m_per_device, k]`` (torch bf16 or uint16 bits);
-    ``y``: bf16 ``[k, n]`` or, with ``rhs_transpose``, ``[n, k]``.
+    ``xs``: P shards ``[m_per_device, k]`` (torch bf16 / fp16 or uint16 bits);
+    ``y``: ``[k, n]`` or, with ``rhs_transpose``, ``[n, k]``, same type.
+    ``dtype`` ("bf16" or "f16") is taken from the torch tensors when omitted.
 
-    acc="f32" returns ``(out_f32, out_bf16_bits)``: float32 sums and their
-    bf16 rounding.  acc="f64" returns the double-precision sums.
+    acc="f32" returns ``(out_f32, out_bits)``: float32 sums and their
+    rounding to the 16-bit type.  acc="f64" returns the double-precision sums.
     """
     lib = lib or load()
-    xb = [as_bf16_bits(x) for x in xs]
-    yb = as_bf16_bits(y)
+    dtype = dtype or _infer_dtype(xs[0])
+    if dtype not in ELEM:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    elem = ELEM[dtype]
+    xb = [as_bits(x, dtype) for x in xs]
+    yb = as_bits(y, dtype)
     P = len(xb)
     m_pd, k = xb[0].shape
     for x in xb:
@@ -123,17 +174,17 @@ def agmm(xs: Sequence, y, rhs_transpose: bool, row_begin: int = 0, row_end: Opti
     ptrs = (u16p * P)(*[x.ctypes.data_as(u16p) for x in xb])
     if acc == "f64":
         out64 = np.empty((rows, n), dtype=np.float64)
-        rc = lib.oracle_agmm(P, m_pd, k, n, int(bool(rhs_transpose)), ptrs, yb.ctypes.data_as(u16p),
-                             row_begin, row_end, 1, None, None,
-                             out64.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), nthreads)
+        rc = lib.oracle_agmm_typed(P, m_pd, k, n, int(bool(rhs_transpose)), ptrs, yb.ctypes.data_as(u16p),
+                                   row_begin, row_end, 1, None, None,
+                                   out64.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), nthreads, elem)
         if rc != 0:
             raise RuntimeError(f"oracle_agmm failed: {rc}")
         return out64
     out32 = np.empty((rows, n), dtype=np.float32)
     out16 = np.empty((rows, n), dtype=np.uint16)
-    rc = lib.oracle_agmm(P, m_pd, k, n, int(bool(rhs_transpose)), ptrs, yb.ctypes.data_as(u16p),
-                         row_begin, row_end, 0, out32.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
-                         out16.ctypes.data_as(u16p), None, nthreads)
+    rc = lib.oracle_agmm_typed(P, m_pd, k, n, int(bool(rhs_transpose)), ptrs, yb.ctypes.data_as(u16p),
+                               row_begin, row_end, 0, out32.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                               out16.ctypes.data_as(u16p), None, nthreads, elem)
     if rc != 0:
         raise RuntimeError(f"oracle_agmm failed: {rc}")
     return out32, out16

@@ -30,6 +30,10 @@
  *    result.
  *  - The float32 -> bf16 cast is round-to-nearest-even; NaN stays NaN.
  *
+ * The same definition with fp16 inputs and output (oracle_agmm_typed): the
+ * element type changes only the two conversions, each written from the IEEE
+ * binary16 layout.
+ *
  * A second accumulation mode sums in double precision.  It is not the pages'
  * arithmetic; the tests use it as a near-exact reference for error bounds.
  *
@@ -70,6 +74,66 @@ uint16_t oracle_f32_to_bf16(float f)
     return (uint16_t)(u >> 16);
 }
 
+/* IEEE-754 binary16 (fp16): 1 sign bit, 5 exponent bits (bias 15), 10
+ * fraction bits.  Exponent 0 encodes zero and the subnormals f * 2^-24;
+ * exponent 31 encodes infinity (fraction 0) and NaN. */
+float oracle_f16_to_f32(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int e = (h >> 10) & 0x1F;
+    const int f = h & 0x3FF;
+    float v;
+    if (e == 0) {
+        v = (float)f * (1.0f / 16777216.0f); /* f * 2^-24, exact in binary32 */
+    } else if (e == 31) {
+        uint32_t u = f ? 0x7FC00000u : 0x7F800000u;
+        memcpy(&v, &u, sizeof v);
+    } else {
+        /* (1024 + f) * 2^(e - 25): build the binary32 pattern directly */
+        uint32_t u = ((uint32_t)(e - 15 + 127) << 23) | ((uint32_t)f << 13);
+        memcpy(&v, &u, sizeof v);
+    }
+    return sign ? -v : v;
+}
+
+/* Round a binary32 value to the nearest fp16, ties to even.  Overflow
+ * rounds to infinity; NaN stays NaN (quiet, sign kept). */
+uint16_t oracle_f32_to_f16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    const int exp = (int)((u >> 23) & 0xFF);
+    const uint32_t frac = u & 0x7FFFFFu;
+    if (exp == 255) return (uint16_t)(sign | (frac ? 0x7E00u : 0x7C00u));
+    if (exp == 0) return sign; /* binary32 zero or subnormal: far below 2^-25 */
+    const int e = exp - 127 + 15; /* fp16 exponent field if the result is normal */
+    if (e >= 31) return (uint16_t)(sign | 0x7C00u);
+    const uint32_t m = frac | 0x800000u; /* 24-bit significand, value m * 2^(exp-150) */
+    /* Units of the result's last place: 2^(e-25) when normal, 2^-24 when subnormal. */
+    const int shift = e >= 1 ? 13 : 14 - e;
+    if (shift > 31) return sign;
+    const uint32_t q = m >> shift;
+    const uint32_t rem = m & ((1u << shift) - 1u);
+    const uint32_t half = 1u << (shift - 1);
+    const uint32_t up = (rem > half || (rem == half && (q & 1u))) ? 1u : 0u;
+    if (e >= 1) {
+        /* q holds the implicit bit at 0x400; a carry into the exponent is correct */
+        return (uint16_t)(sign | (uint32_t)(((uint32_t)(e - 1) << 10) + q + up));
+    }
+    return (uint16_t)(sign | (q + up)); /* subnormal; a carry makes the smallest normal */
+}
+
+void oracle_f16_array_to_f32(const uint16_t *src, float *dst, int64_t count)
+{
+    for (int64_t i = 0; i < count; ++i) dst[i] = oracle_f16_to_f32(src[i]);
+}
+
+void oracle_f32_array_to_f16(const float *src, uint16_t *dst, int64_t count)
+{
+    for (int64_t i = 0; i < count; ++i) dst[i] = oracle_f32_to_f16(src[i]);
+}
+
 void oracle_bf16_array_to_f32(const uint16_t *src, float *dst, int64_t count)
 {
     for (int64_t i = 0; i < count; ++i) dst[i] = oracle_bf16_to_f32(src[i]);
@@ -94,11 +158,45 @@ void oracle_f32_array_to_bf16(const float *src, uint16_t *dst, int64_t count)
  *
  * Returns 0 on success, -1 on invalid arguments, -2 on allocation failure.
  */
+/* Element types of the 16-bit inputs and output. */
+enum { ORACLE_BF16 = 0, ORACLE_F16 = 1 };
+
+static float elem_to_f32(uint16_t b, int elem)
+{
+    return elem == ORACLE_F16 ? oracle_f16_to_f32(b) : oracle_bf16_to_f32(b);
+}
+
+static uint16_t f32_to_elem(float f, int elem)
+{
+    return elem == ORACLE_F16 ? oracle_f32_to_f16(f) : oracle_f32_to_bf16(f);
+}
+
+/*
+ * The same product with the element type of X, Y and the 16-bit output given
+ * by `elem` (ORACLE_BF16 or ORACLE_F16); out_bf16 then receives that type's
+ * bit patterns.  Products of two fp16 values (11-bit significands) are also
+ * exact in float32.
+ */
+int oracle_agmm_typed(int P, int64_t m_per_device, int64_t k, int64_t n, int rhs_transpose,
+                      const uint16_t *const *x_shards, const uint16_t *y,
+                      int64_t row_begin, int64_t row_end, int acc_double,
+                      float *out_f32, uint16_t *out_bf16, double *out_f64, int nthreads, int elem);
+
 int oracle_agmm(int P, int64_t m_per_device, int64_t k, int64_t n, int rhs_transpose,
                 const uint16_t *const *x_shards, const uint16_t *y,
                 int64_t row_begin, int64_t row_end, int acc_double,
                 float *out_f32, uint16_t *out_bf16, double *out_f64, int nthreads)
 {
+    return oracle_agmm_typed(P, m_per_device, k, n, rhs_transpose, x_shards, y, row_begin, row_end,
+                             acc_double, out_f32, out_bf16, out_f64, nthreads, ORACLE_BF16);
+}
+
+int oracle_agmm_typed(int P, int64_t m_per_device, int64_t k, int64_t n, int rhs_transpose,
+                      const uint16_t *const *x_shards, const uint16_t *y,
+                      int64_t row_begin, int64_t row_end, int acc_double,
+                      float *out_f32, uint16_t *out_bf16, double *out_f64, int nthreads, int elem)
+{
+    if (elem != ORACLE_BF16 && elem != ORACLE_F16) return -1;
     if (P < 1 || m_per_device < 1 || k < 1 || n < 1 || !x_shards || !y) return -1;
     const int64_t M = (int64_t)P * m_per_device;
     if (row_begin < 0 || row_end > M || row_begin > row_end) return -1;
@@ -122,11 +220,11 @@ int oracle_agmm(int P, int64_t m_per_device, int64_t k, int64_t n, int rhs_trans
     for (int64_t i = 0; i < rows; ++i) {
         const int64_t g = row_begin + i;
         const uint16_t *src = x_shards[g / m_per_device] + (g % m_per_device) * k;
-        for (int64_t kk = 0; kk < k; ++kk) xcat[i * k + kk] = oracle_bf16_to_f32(src[kk]);
+        for (int64_t kk = 0; kk < k; ++kk) xcat[i * k + kk] = elem_to_f32(src[kk], elem);
     }
     for (int64_t kk = 0; kk < k; ++kk)
         for (int64_t j = 0; j < n; ++j)
-            ycan[kk * n + j] = oracle_bf16_to_f32(rhs_transpose ? y[j * k + kk] : y[kk * n + j]);
+            ycan[kk * n + j] = elem_to_f32(rhs_transpose ? y[j * k + kk] : y[kk * n + j], elem);
 
     int failed = 0;
 #ifdef _OPENMP
@@ -159,9 +257,9 @@ int oracle_agmm(int P, int64_t m_per_device, int64_t k, int64_t n, int rhs_trans
                 const float *yr = ycan + kk * n;
                 for (int64_t j = 0; j < n; ++j) acc[j] += a * yr[j];
             }
-            /* Step 4: cast to the output dtype (bf16, round to nearest even). */
+            /* Step 4: cast to the output dtype (bf16 or fp16, round to nearest even). */
             if (out_bf16)
-                for (int64_t j = 0; j < n; ++j) out_bf16[i * n + j] = oracle_f32_to_bf16(acc[j]);
+                for (int64_t j = 0; j < n; ++j) out_bf16[i * n + j] = f32_to_elem(acc[j], elem);
             if (!out_f32) free(acc);
         }
     }

@@ -6,6 +6,9 @@ planted mistake and show that every mistake is caught.
 
 Pins:
   * bf16 rounding: hand-worked bit patterns (tests/golden/bf16_rounding.json)
+  * fp16 rounding and decoding: hand-worked bit patterns
+    (tests/golden/f16_rounding.json), PyTorch's casts, and the fp16 product
+    by the same invariants as the bf16 one
     and agreement with PyTorch's float32 -> bfloat16 cast (a library routine).
   * a hand-worked example (tests/golden/hand_example.json), both layouts.
   * P = 1 reduces to a plain matmul: checked against torch.matmul in float64
@@ -255,9 +258,159 @@ def pin_row_range(lib):
         assert np.array_equal(p32, full32[r0:r1]) and np.array_equal(p16, full16[r0:r1])
 
 
+# ----------------------------------------------------------------------------- fp16 pins
+# The fp16 variant changes only the two conversions; these pin them, and the
+# product with fp16 operands, against the binary16 layout, PyTorch's casts
+# and exact arithmetic.
+
+def _f16_cat_f64(xs):
+    # decoded by PyTorch, independently of the oracle
+    return np.concatenate([x.float().double().numpy() for x in xs])
+
+
+def _f16_ycan_f64(y, rt):
+    yf = y.float().double().numpy()
+    return yf.T if rt else yf
+
+
+def pin_f16_golden(lib):
+    with open(os.path.join(GOLDEN, "f16_rounding.json")) as f:
+        g = json.load(f)
+    for f32hex, f16hex, why in g["encode"]:
+        f = np.array([int(f32hex, 16)], dtype=np.uint32).view(np.float32)
+        got = int(oracle.f32_to_f16_bits(f, lib)[0])
+        assert got == int(f16hex, 16), (f32hex, hex(got), why)
+    for f16hex, f32hex, why in g["decode"]:
+        got = oracle.f16_bits_to_f32(np.array([int(f16hex, 16)], dtype=np.uint16), lib).view(np.uint32)[0]
+        assert int(got) == int(f32hex, 16), (f16hex, hex(int(got)), why)
+    for nan_bits in (0x7FC00000, 0x7F800001, 0xFFC00001):
+        f = np.array([nan_bits], dtype=np.uint32).view(np.float32)
+        got = int(oracle.f32_to_f16_bits(f, lib)[0])
+        assert (got & 0x7C00) == 0x7C00 and (got & 0x03FF) != 0, hex(got)
+
+
+def pin_f16_vs_torch(lib):
+    rng = np.random.default_rng(4321)
+    # random signs, fractions and exponents spanning fp16's subnormals to overflow
+    nrand = 200_000
+    exp = rng.integers(127 - 30, 127 + 18, size=nrand).astype(np.uint32)
+    frac = rng.integers(0, 1 << 23, size=nrand).astype(np.uint32)
+    sign = rng.integers(0, 2, size=nrand).astype(np.uint32)
+    f = ((sign << 31) | (exp << 23) | frac).view(np.float32)
+    # exact ties: normal range (discarded 13 bits = 0x1000) and subnormal range
+    te = rng.integers(127 - 14, 127 + 16, size=20_000).astype(np.uint32)
+    tf = rng.integers(0, 1 << 10, size=20_000).astype(np.uint32)
+    ties_n = ((te << 23) | (tf << 13) | 0x1000).view(np.float32)
+    ties_s = (rng.integers(0, 1 << 11, size=20_000).astype(np.float32) + 0.5) * np.float32(2.0 ** -24)
+    f = np.concatenate([f, ties_n, ties_s, -ties_s])
+    ours = oracle.f32_to_f16_bits(f, lib)
+    ref = torch.from_numpy(f.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    bad = np.nonzero(ours != ref)[0]
+    assert bad.size == 0, [(hex(int(f.view(np.uint32)[i])), hex(int(ours[i])), hex(int(ref[i]))) for i in bad[:5]]
+    # every fp16 pattern decodes as PyTorch decodes it
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    dec = oracle.f16_bits_to_f32(allb, lib)
+    tref = torch.from_numpy(allb.view(np.int16).copy()).view(torch.float16).float().numpy()
+    nan = np.isnan(tref)
+    assert np.array_equal(np.isnan(dec), nan)
+    assert np.array_equal(dec[~nan].view(np.uint32), tref[~nan].view(np.uint32))
+
+
+def pin_f16_plain_matmul_p1(lib):
+    for (m, k, n, rt, dist) in [(7, 64, 24, False, "uniform"), (5, 256, 40, True, "normal"),
+                                (33, 130, 17, False, "normal")]:
+        xs, y = make_inputs(1, m, k, n, rt, dist=dist, seed=27, dtype="f16")
+        o32, _ = oracle.agmm(xs, y, rt, lib=lib)
+        a = _f16_cat_f64(xs)
+        b = _f16_ycan_f64(y, rt)
+        ref = (torch.from_numpy(a) @ torch.from_numpy(b)).numpy()
+        bound = gamma(k) * (np.abs(a) @ np.abs(b)) + 1e-30
+        err = np.abs(o32.astype(np.float64) - ref)
+        assert np.all(err <= bound), (m, k, n, rt, float((err / bound).max()))
+        assert np.any(err > 0)
+
+
+def pin_f16_identity_embedding(lib):
+    for rt in (False, True):
+        P, m, k, n = 3, 5, 48, 32
+        xs, _ = make_inputs(P, m, k, n, rt, dist="normal", seed=33, dtype="f16")
+        eye = torch.zeros((k, n), dtype=torch.float32)
+        eye[:n, :n] = torch.eye(n)
+        y = (eye.T.contiguous() if rt else eye).to(torch.float16)
+        o32, o16 = oracle.agmm(xs, y, rt, lib=lib)
+        xcat = np.concatenate([oracle.as_bits(x, "f16") for x in xs])
+        assert np.array_equal(o16, xcat[:, :n]), rt
+        assert np.array_equal(o32, np.concatenate([x.float().numpy() for x in xs])[:, :n]), rt
+
+
+_F16_TABLE = None
+
+
+def _f16_finite_table():
+    """Every finite fp16 value as an exact Fraction, sorted, with its bits
+    (from PyTorch's decoding)."""
+    global _F16_TABLE
+    if _F16_TABLE is None:
+        allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+        vals = torch.from_numpy(allb.view(np.int16).copy()).view(torch.float16).double().numpy()
+        pairs = {}
+        for b, v in zip(allb.tolist(), vals.tolist()):
+            if np.isfinite(v) and not (v == 0.0 and b == 0x8000):
+                pairs[Fraction(v)] = b
+        keys = sorted(pairs)
+        _F16_TABLE = (keys, [pairs[q] for q in keys])
+    return _F16_TABLE
+
+
+def _rne_exact_f16(v: Fraction):
+    """Round an exact value to fp16, ties to even; returns (bits, midpoint or None)."""
+    import bisect
+
+    keys, bits = _f16_finite_table()
+    i = bisect.bisect_left(keys, v)
+    if i < len(keys) and keys[i] == v:
+        return bits[i], None
+    lo, hi = i - 1, i
+    dl, dh = v - keys[lo], keys[hi] - v
+    mid = (keys[lo] + keys[hi]) / 2
+    if dl < dh:
+        return bits[lo], mid
+    if dh < dl:
+        return bits[hi], mid
+    return (bits[lo] if (bits[lo] & 1) == 0 else bits[hi]), mid
+
+
+def pin_f16_bruteforce_exact(lib):
+    rng = np.random.default_rng(47)
+    for trial in range(5):
+        P = int(rng.integers(1, 4))
+        m = int(rng.integers(1, 5))
+        k = int(rng.integers(1, 33))
+        n = int(rng.integers(1, 17))
+        rt = bool(trial % 2)
+        xs, y = make_inputs(P, m, k, n, rt, dist="uniform", seed=200 + trial, dtype="f16")
+        o32, o16 = oracle.agmm(xs, y, rt, lib=lib)
+        a = [[Fraction(float(v)) for v in row] for row in _f16_cat_f64(xs)]
+        bf = [[Fraction(float(v)) for v in row] for row in _f16_ycan_f64(y, rt)]
+        for i in range(P * m):
+            for j in range(n):
+                exact = sum((a[i][kk] * bf[kk][j] for kk in range(k)), Fraction(0))
+                absum = sum((abs(a[i][kk] * bf[kk][j]) for kk in range(k)), Fraction(0))
+                bound = Fraction(gamma(k)) * absum
+                assert abs(Fraction(float(o32[i, j])) - exact) <= bound, (trial, i, j)
+                if exact == 0:
+                    assert float(o32[i, j]) == 0.0
+                    continue
+                want, mid = _rne_exact_f16(exact)
+                if mid is None or abs(exact - mid) > bound:
+                    assert int(o16[i, j]) == want, (trial, i, j, hex(int(o16[i, j])), hex(want))
+
+
 ALL_PINS = [pin_bf16_golden, pin_bf16_vs_torch, pin_hand_example, pin_plain_matmul_p1,
             pin_identity_embedding, pin_shard_isolation, pin_shard_permutation, pin_scale_by_two,
-            pin_bruteforce_exact, pin_layout_consistency, pin_double_mode_close, pin_row_range]
+            pin_bruteforce_exact, pin_layout_consistency, pin_double_mode_close, pin_row_range,
+            pin_f16_golden, pin_f16_vs_torch, pin_f16_plain_matmul_p1, pin_f16_identity_embedding,
+            pin_f16_bruteforce_exact]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
@@ -306,6 +459,12 @@ MUTANTS = {
     "round_half_up": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0x8000u;"),
     "truncating_cast": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u;"),
     "wrong_row_in_shard": ("(g % m_per_device) * k", "(g / P % m_per_device) * k"),
+    # the fp16 conversions
+    "f16_round_half_up": ("(rem > half || (rem == half && (q & 1u)))", "(rem >= half)"),
+    "f16_truncating_cast": ("(rem > half || (rem == half && (q & 1u)))", "(0)"),
+    "f16_subnormal_scale": ("const int shift = e >= 1 ? 13 : 14 - e;", "const int shift = e >= 1 ? 13 : 13 - e;"),
+    "f16_no_overflow": ("if (e >= 31) return (uint16_t)(sign | 0x7C00u);", "if (e >= 32) return (uint16_t)(sign | 0x7C00u);"),
+    "f16_decode_bias": ("((uint32_t)(e - 15 + 127) << 23)", "((uint32_t)(e - 16 + 127) << 23)"),
 }
 
 
