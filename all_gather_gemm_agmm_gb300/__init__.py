@@ -26,6 +26,8 @@ AGMM_ERR_TIMEOUT = 5
 AGMM_ERR_NOMEM = 6
 AGMM_BF16 = 0
 AGMM_BF16_F32OUT = 1
+AGMM_F16 = 2
+AGMM_F16_F32OUT = 3
 
 # Every symbol agmm.h declares.
 EXPORTED_SYMBOLS = [
@@ -146,14 +148,18 @@ class Plan:
     """A planned problem: P shards of [m_per_device, k] times Y ([k, n] or [n, k])."""
 
     def __init__(self, P: int, m_per_device: int, k: int, n: int, rhs_transpose: bool = False,
-                 out_f32: bool = False):
+                 out_f32: bool = False, f16: bool = False):
         self._lib = load_library()
         self.P, self.m_per_device, self.k, self.n = int(P), int(m_per_device), int(k), int(n)
         self.rhs_transpose = bool(rhs_transpose)
         self.out_f32 = bool(out_f32)
+        self.f16 = bool(f16)
+        if self.f16:
+            dtype = AGMM_F16_F32OUT if out_f32 else AGMM_F16
+        else:
+            dtype = AGMM_BF16_F32OUT if out_f32 else AGMM_BF16
         h = ctypes.c_void_p()
-        _check(self._lib.agmm_plan(self.P, self.m_per_device, self.k, self.n,
-                                   AGMM_BF16_F32OUT if out_f32 else AGMM_BF16, int(self.rhs_transpose),
+        _check(self._lib.agmm_plan(self.P, self.m_per_device, self.k, self.n, dtype, int(self.rhs_transpose),
                                    ctypes.byref(h)))
         self._h = h
 
@@ -236,9 +242,11 @@ def _check_operands(xs, y, rhs_transpose: bool):
     if len(xs) < 1:
         raise ValueError("need at least one shard")
     m, k = xs[0].shape
+    if xs[0].dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("inputs must be bfloat16 or float16")
     for x in xs:
-        if x.dtype != torch.bfloat16 or y.dtype != torch.bfloat16:
-            raise ValueError("inputs must be bfloat16")
+        if x.dtype != xs[0].dtype or y.dtype != xs[0].dtype:
+            raise ValueError("shards and y must share one dtype")
         if x.shape != (m, k) or not x.is_contiguous() or not x.is_cuda:
             raise ValueError("shards must be contiguous CUDA tensors of one shape")
     if y.dim() != 2 or not y.is_contiguous() or not y.is_cuda:
@@ -254,17 +262,19 @@ _plan_cache: Dict[tuple, Plan] = {}
 
 def all_gather_matmul(xs, y, my_id: int = 0, rhs_transpose: bool = False, out=None, unfused: bool = False,
                       out_f32: bool = False, workspace=None, stream=None):
-    """all-gather(xs, axis=0) @ y on one GPU; returns O [P*m, n] (bf16 or float32)."""
+    """all-gather(xs, axis=0) @ y on one GPU; returns O [P*m, n] in the input
+    dtype (bf16 or fp16) or float32."""
     import torch
 
     m, k, n = _check_operands(xs, y, rhs_transpose)
-    key = (len(xs), m, k, n, bool(rhs_transpose), bool(out_f32), torch.cuda.current_device())
+    f16 = xs[0].dtype == torch.float16
+    key = (len(xs), m, k, n, bool(rhs_transpose), bool(out_f32), f16, torch.cuda.current_device())
     plan = _plan_cache.get(key)
     if plan is None:
-        plan = Plan(len(xs), m, k, n, rhs_transpose, out_f32)
+        plan = Plan(len(xs), m, k, n, rhs_transpose, out_f32, f16)
         _plan_cache[key] = plan
     if out is None:
-        out = torch.empty((plan.M, n), dtype=torch.float32 if out_f32 else torch.bfloat16, device=y.device)
+        out = torch.empty((plan.M, n), dtype=torch.float32 if out_f32 else xs[0].dtype, device=y.device)
     if workspace is None:
         workspace = plan.new_workspace(unfused, device=y.device)
     (plan.run_unfused if unfused else plan.run)(xs, y, out, my_id, workspace, stream)

@@ -76,7 +76,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
 bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-               uint32_t box_outer, std::string* err) {
+               uint32_t box_outer, bool f16, std::string* err) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) {
     *err = "cuTensorMapEncodeTiled is not available from the driver";
@@ -86,7 +86,7 @@ bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+  CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -117,6 +117,7 @@ struct agmm_plan_s {
   int max_clusters = 0;  // co-resident clusters (rows path)
   bool swap_dsmem = false;  // swap path: k-split partials through DSMEM
   int row_groups = 1;       // swap path: row groups of the gathered rows (grid z)
+  bool f16 = false;         // fp16 operands (else bf16)
   int clock_khz = 2100000;  // peak SM clock of the planned device
   int group_chunks = 0;     // swap path: ring chunks per row group
   size_t tail_bytes = 0;  // workspace bytes for tail counters and partials
@@ -146,7 +147,7 @@ agmm_status_t validate_shape(int P, int64_t m_pd, int64_t k, int64_t n, int dtyp
   const int64_t M = (int64_t)P * m_pd;
   if (M > kMaxElems / k || k > kMaxElems / n || M > kMaxElems / n)
     return fail(AGMM_ERR_INVALID_ARG, "problem exceeds 2^40 elements in an operand");
-  if (dtype != AGMM_BF16 && dtype != AGMM_BF16_F32OUT) return fail(AGMM_ERR_INVALID_ARG, "unknown dtype");
+  if (dtype < AGMM_BF16 || dtype > AGMM_F16_F32OUT) return fail(AGMM_ERR_INVALID_ARG, "unknown dtype");
   if (rhs_t != 0 && rhs_t != 1) return fail(AGMM_ERR_INVALID_ARG, "rhs_transpose must be 0 or 1");
   return AGMM_OK;
 }
@@ -332,7 +333,8 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   pl->num_sms = sms;
   pl->clock_khz = clock_khz;
   pl->key.y_kmajor = rhs_t != 0;
-  pl->key.out_f32 = dtype == AGMM_BF16_F32OUT;
+  pl->key.out_f32 = dtype == AGMM_BF16_F32OUT || dtype == AGMM_F16_F32OUT;
+  pl->f16 = dtype == AGMM_F16 || dtype == AGMM_F16_F32OUT;
   pl->out_elem = pl->key.out_f32 ? 4 : 2;
   st = choose_tiles(pl);
   if (st != AGMM_OK) {
@@ -452,6 +454,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.wait_limit_cycles = (uint64_t)std::max(1, env_int("AGMM_WAIT_LIMIT_MS", 2000)) * (uint64_t)pl->clock_khz;
   kp.test_drop_first_arrive = env_int("AGMM_TEST_DROP_ARRIVE", 0) != 0;
   kp.pdl = env_int("AGMM_PDL", 1) != 0;
+  kp.f16 = pl->f16 ? 1 : 0;
   kp.dp_tiles = pl->dp_tiles;
   if (with_sub && P > 1) {
     st = plan_impl(1, pl->M(), k, n, dtype, rhs_t, false, &pl->sub);
@@ -493,7 +496,7 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
   if (!same) {
     std::string err;
     for (int r = 0; r < pl->P; ++r) {
-      if (!encode_2d(&kp.xmap[r], xs[r], (uint64_t)pl->k, (uint64_t)pl->m_pd, kTileK, (uint32_t)pl->box_rows, &err)) {
+      if (!encode_2d(&kp.xmap[r], xs[r], (uint64_t)pl->k, (uint64_t)pl->m_pd, kTileK, (uint32_t)pl->box_rows, pl->f16, &err)) {
         pl->cache_valid = false;
         return fail(AGMM_ERR_CUDA, "shard tensor map: " + err);
       }
@@ -502,9 +505,9 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
     const uint32_t y_rows =
         pl->key.path == kPathSwap ? (uint32_t)kTileM : (uint32_t)(pl->key.bn / pl->key.cm);
     if (pl->rhs_t)  // Y [n, k]: K-major boxes of y_rows n-rows
-      ok = encode_2d(&kp.ymap, y, (uint64_t)pl->k, (uint64_t)pl->n, kTileK, y_rows, &err);
+      ok = encode_2d(&kp.ymap, y, (uint64_t)pl->k, (uint64_t)pl->n, kTileK, y_rows, pl->f16, &err);
     else  // Y [k, n]: MN-major boxes of 64 n x 64 k
-      ok = encode_2d(&kp.ymap, y, (uint64_t)pl->n, (uint64_t)pl->k, 64, kTileK, &err);
+      ok = encode_2d(&kp.ymap, y, (uint64_t)pl->n, (uint64_t)pl->k, 64, kTileK, pl->f16, &err);
     if (!ok) {
       pl->cache_valid = false;
       return fail(AGMM_ERR_CUDA, "Y tensor map: " + err);

@@ -29,6 +29,7 @@
 // status words; all roles then leave their loops, wait (bounded) for their own
 // TMA and MMA work in flight, and the CTA frees its tensor memory and returns.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernel_params.h"
 #include "ptx_sm103.cuh"
@@ -209,7 +210,13 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+// Two float32 values rounded (to nearest even) to the 16-bit output type:
+// bf16, or fp16 when f16.
+__device__ __forceinline__ uint32_t pack_16x2(float lo, float hi, bool f16) {
+  if (f16) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
@@ -217,28 +224,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Store 32 consecutive f32 accumulator values of one output row.
 template <bool kF32>
 __device__ __forceinline__ void store_row32(void* out, int64_t ldo, int64_t row, int64_t col,
-                                            const uint32_t (&v)[32]) {
+                                            const uint32_t (&v)[32], bool f16) {
   if constexpr (kF32) {
     uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(out) + row * ldo + col);
 #pragma unroll
     for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
   } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row * ldo + col);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row * ldo + col);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
-                          pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                          pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                          pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+      dst[i] = make_uint4(pack_16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]), f16),
+                          pack_16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]), f16),
+                          pack_16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]), f16),
+                          pack_16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]), f16));
     }
   }
 }
 
 // Store one value.
 template <bool kF32>
-__device__ __forceinline__ void store_one(void* out, int64_t ldo, int64_t row, int64_t col, float v) {
+__device__ __forceinline__ void store_one(void* out, int64_t ldo, int64_t row, int64_t col, float v, bool f16) {
   if constexpr (kF32) {
     static_cast<float*>(out)[row * ldo + col] = v;
+  } else if (f16) {
+    static_cast<__half*>(out)[row * ldo + col] = __float2half_rn(v);
   } else {
     static_cast<__nv_bfloat16*>(out)[row * ldo + col] = __float2bfloat16_rn(v);
   }
@@ -247,12 +256,12 @@ __device__ __forceinline__ void store_one(void* out, int64_t ldo, int64_t row, i
 // Store 4 consecutive values of one output row.
 template <bool kF32>
 __device__ __forceinline__ void store_row4(void* out, int64_t ldo, int64_t row, int64_t col,
-                                           float4 s) {
+                                           float4 s, bool f16) {
   if constexpr (kF32) {
     *reinterpret_cast<float4*>(static_cast<float*>(out) + row * ldo + col) = s;
   } else {
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + row * ldo + col) =
-        make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + row * ldo + col) =
+        make_uint2(pack_16x2(s.x, s.y, f16), pack_16x2(s.z, s.w, f16));
   }
 }
 
@@ -309,7 +318,7 @@ __device__ __forceinline__ void owner_sum_global(const KernelParams& p, const Ow
           const int cj = q * 4 + j;
           const int4 e = os.chunk_tab[os.c0 + (cj >> p.box_shift)];
           const int r = cj & (p.box_rows - 1);
-          if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j]);
+          if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j], p.f16 != 0);
         }
       }
     }
@@ -594,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       const bool a_mn = (kPath == kPathSwap) && !kYK;
       const bool b_mn = (kPath == kPathRows) && !kYK;
       // a pair MMA spans both CTAs' 128 rows: M = 256
-      const uint32_t idesc = ptx::idesc_bf16_f32(kPair ? 2 * kTileM : kTileM, mma_n, a_mn, b_mn);
+      const uint32_t idesc = ptx::idesc_f16kind_f32(kPair ? 2 * kTileM : kTileM, mma_n, a_mn, b_mn, p.f16 != 0);
       constexpr uint16_t kPairMask = 3;
       int stage = 0;
       uint32_t phase = 0;
@@ -812,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
               }
             }
           }
-          if (out_row >= 0) store_row32<kF32>(p.out, p.ldo, out_row, (int64_t)sg.nt * kBN + c * 32, v);
+          if (out_row >= 0) store_row32<kF32>(p.out, p.ldo, out_row, (int64_t)sg.nt * kBN + c * 32, v, p.f16 != 0);
         }
         if (sg.role == kSegContrib) {
           // Publish: every thread fences its stores and arrives; one thread
@@ -994,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           if (cj < c1) {
             const int4 e = chunk_tab[swap_c0 + (cj >> p.box_shift)];
             const int r = cj & (p.box_rows - 1);
-            if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j]);
+            if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j], p.f16 != 0);
           }
         }
       }

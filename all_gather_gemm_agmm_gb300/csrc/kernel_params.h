@@ -71,6 +71,7 @@ struct __align__(128) KernelParams {
   float* swap_partials;
   int group_chunks;  // swap path: ring chunks per row group (blockIdx.z)
   int pdl;  // launched with programmatic stream serialization (host side only)
+  int f16;  // X, Y and a 16-bit O are fp16 (else bf16)
 };
 
 struct GatherParams {

@@ -282,15 +282,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B and f32 D: D format bits
-// 4-5 = 1 (f32), A format bits 7-9 = 1 (bf16), B format bits 10-12 = 1 (bf16),
-// A/B major bits 15/16 (0 = K-major, 1 = MN-major), N >> 3 at bits 17-22,
-// M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16 with f32 D: D format bits 4-5 = 1
+// (f32), A and B format bits 7-9 and 10-12 = 1 (bf16) or 0 (fp16), A/B major
+// bits 15/16 (0 = K-major, 1 = MN-major), N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                         bool f16) {
+  // A and B formats (bits 7-9, 10-12): 0 = F16, 1 = BF16; both operands of
+  // one MMA have the same type.
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------- clusters

@@ -194,8 +194,10 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- our arm
-def build_replicas(w, R, device, seed=1234):
+def build_replicas(w, R, device, seed=1234, dtype="bf16"):
     import torch
+
+    tdt = torch.float16 if dtype == "f16" else torch.bfloat16
 
     reps = []
     g = torch.Generator(device=device)
@@ -207,11 +209,11 @@ def build_replicas(w, R, device, seed=1234):
                 t = torch.rand(shape, generator=g, device=device, dtype=torch.float32) * 2 - 1
             else:
                 t = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std
-            return t.to(torch.bfloat16)
+            return t.to(tdt)
 
         xs = [draw((w.m_per_device, w.k), 1.0) for _ in range(w.P)]
         y = draw((w.n, w.k) if w.rhs_transpose else (w.k, w.n), 0.02)
-        o = torch.empty((w.M, w.n), dtype=torch.bfloat16, device=device)
+        o = torch.empty((w.M, w.n), dtype=tdt, device=device)
         reps.append((xs, y, o))
     return reps
 
@@ -260,12 +262,12 @@ def run_timed(graph, step_fns, K, stream, sampler=None):
     return start.elapsed_time(end) / 1000.0, clocks
 
 
-def cpu_oracle_sample(w, target_s=8.0):
+def cpu_oracle_sample(w, target_s=8.0, dtype="bf16"):
     """The oracle as it stands, on a bounded sample of the workload's rows."""
     import oracle
-    from all_gather_gemm_agmm_gb300.inputs import make_workload_inputs
+    from all_gather_gemm_agmm_gb300.inputs import make_inputs
 
-    xs, y = make_workload_inputs(w)
+    xs, y = make_inputs(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, w.dist, w.seed, dtype=dtype)
     rows_total = w.M
     lib = oracle.load()
     # calibrate on a block of rows, then size each call to about a second
@@ -302,8 +304,8 @@ def bench_ours(args, w):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size or L2_BYTES_FALLBACK
     per_rep = w.unique_bytes
     R = max(2, -(-3 * l2 // per_rep))
-    reps = build_replicas(w, R, device)
-    plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose)
+    reps = build_replicas(w, R, device, dtype=args.dtype)
+    plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, f16=args.dtype == "f16")
     info = plan.info()
     ws = plan.new_workspace(False, device=device)
     ws_unf = plan.new_workspace(True, device=device)
@@ -352,10 +354,11 @@ def bench_ours(args, w):
         slots = []
         for si in range(2):
             xs_d, y_d, o_d = reps[si % len(reps)]
-            pl = plan if si == 0 else agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose)
+            pl = plan if si == 0 else agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose,
+                                                f16=args.dtype == "f16")
             wsi = ws if si == 0 else pl.new_workspace()
             st = stream if si == 0 else torch.cuda.Stream(device=device)
-            slots.append((pl, wsi, st, xs_d, y_d, o_d, torch.empty((w.M, w.n), dtype=torch.bfloat16).pin_memory()))
+            slots.append((pl, wsi, st, xs_d, y_d, o_d, torch.empty((w.M, w.n), dtype=o_d.dtype).pin_memory()))
         torch.cuda.synchronize()
         Ke = max(3, min(K, 200 if w.unique_bytes < 1e9 else 20))
 
@@ -411,7 +414,7 @@ def bench_ours(args, w):
     result = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_n, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded torch.Generator on device; shapes of the workload)",
+        "dtype": args.dtype, "data": "synthetic (seeded torch.Generator on device; shapes of the workload)",
         "config": {"workload": w.name, "P": w.P, "m_per_device": w.m_per_device, "k": w.k, "n": w.n,
                    "rhs_transpose": w.rhs_transpose, "my_id": w.my_id, "dist": w.dist,
                    "l2": f"{R} rotating input/output replicas, {R * per_rep / 2**20:.0f} MiB > 3x L2 "
@@ -426,7 +429,7 @@ def bench_ours(args, w):
         "clocks": clocks,
     }
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_oracle_sample(w, target_s=args.cpu_seconds)
+        result["cpu_baseline"] = cpu_oracle_sample(w, target_s=args.cpu_seconds, dtype=args.dtype)
     if rank == 0:
         print(json.dumps(result), flush=True)
 
@@ -445,8 +448,8 @@ def bench_sweep(args):
     stream = torch.cuda.Stream(device=device)
     for w in SWEEP:
         R = max(2, -(-3 * l2 // w.unique_bytes))
-        reps = build_replicas(w, R, device)
-        plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose)
+        reps = build_replicas(w, R, device, dtype=args.dtype)
+        plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, f16=args.dtype == "f16")
         ws = plan.new_workspace(False, device=device)
         wsu = plan.new_workspace(True, device=device)
         torch.cuda.synchronize()  # zeroed workspaces and inputs before launches on `stream`
@@ -478,9 +481,9 @@ def bench_reference(args, w):
     if ws_n > 1 and rank != 0:
         return
     import oracle
-    from all_gather_gemm_agmm_gb300.inputs import make_workload_inputs
+    from all_gather_gemm_agmm_gb300.inputs import make_inputs
 
-    xs, y = make_workload_inputs(w)
+    xs, y = make_inputs(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, w.dist, w.seed, dtype=args.dtype)
     lib = oracle.load()
     cal = min(w.M, 32)
     t0 = time.perf_counter()
@@ -520,6 +523,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true", help="fused vs unfused at every sweep point")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
+                    help="element type of X, Y and O (fp16: the tutorial's float16 variant)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)

@@ -18,8 +18,9 @@
  * writes row block r of O at rows [r*m_per_device, (r+1)*m_per_device).  The
  * gathered left-hand side is never written to device memory by agmm_run.
  *
- * Layout: every matrix is dense row-major bf16.  O is [P*m_per_device, n],
- * bf16 (AGMM_BF16) or float32 (AGMM_BF16_F32OUT).
+ * Layout: every matrix is dense row-major bf16 (AGMM_BF16*) or fp16
+ * (AGMM_F16*; the AllGather-GEMM tutorial's float16 tensors).  O is
+ * [P*m_per_device, n] in the input type, or float32 (the *_F32OUT types).
  *
  * Ownership: the caller owns every device buffer (shards, Y, O, workspace)
  * and the stream.  A plan owns host memory only.
@@ -58,7 +59,9 @@ typedef enum {
 
 typedef enum {
   AGMM_BF16 = 0,        /* bf16 inputs, float32 accumulation, bf16 output    */
-  AGMM_BF16_F32OUT = 1  /* bf16 inputs, float32 accumulation, float32 output */
+  AGMM_BF16_F32OUT = 1, /* bf16 inputs, float32 accumulation, float32 output */
+  AGMM_F16 = 2,         /* fp16 inputs, float32 accumulation, fp16 output    */
+  AGMM_F16_F32OUT = 3   /* fp16 inputs, float32 accumulation, float32 output */
 } agmm_dtype_t;
 
 typedef struct agmm_plan_s* agmm_plan_t;

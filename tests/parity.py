@@ -9,6 +9,9 @@ Tolerance (bf16 inputs, float32 accumulation):
     cannot be closer to the float32 sum than half an ulp (0.03 for values in
     [8, 16)), and two correct float32 sums that straddle a rounding midpoint
     round one ulp apart, so the per-element bound is "2e-2 or one bf16 ulp".
+  * fp16 output (fp16 inputs): the same gate with the fp16 ulp.  fp16 keeps
+    11 significant bits, so below 32 the literal 2e-2 bound is the one that
+    applies.
 """
 import numpy as np
 import torch
@@ -27,9 +30,16 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(a)) - 7)
 
 
+def f16_ulp(x: np.ndarray) -> np.ndarray:
+    a = np.abs(x.astype(np.float64))
+    a = np.where(a < 2.0 ** -14, 2.0 ** -14, a)
+    return 2.0 ** (np.floor(np.log2(a)) - 10)
+
+
 def to_device_guarded(t: torch.Tensor, device="cuda"):
-    """Copy a 2-D bf16 tensor into a fresh allocation with NaN rows before and
-    after it; returns (view of the payload, the whole buffer)."""
+    """Copy a 2-D bf16 or fp16 tensor into a fresh allocation with NaN rows
+    before and after it (0x7fc0 is a NaN in both types); returns (view of the
+    payload, the whole buffer)."""
     rows, cols = t.shape
     buf = torch.empty((rows + 2 * GUARD_ROWS, cols), dtype=t.dtype, device=device)
     buf.view(torch.int16).fill_(BF16_NAN)
@@ -38,8 +48,8 @@ def to_device_guarded(t: torch.Tensor, device="cuda"):
     return view, buf
 
 
-def alloc_output_guarded(M, n, f32=False, device="cuda"):
-    dt = torch.float32 if f32 else torch.bfloat16
+def alloc_output_guarded(M, n, f32=False, device="cuda", f16=False):
+    dt = torch.float32 if f32 else (torch.float16 if f16 else torch.bfloat16)
     buf = torch.full((M + 2 * GUARD_ROWS, n), float("nan"), dtype=dt, device=device)
     return buf[GUARD_ROWS:GUARD_ROWS + M], buf
 
@@ -61,7 +71,8 @@ def check(gpu_out: torch.Tensor, ref32: np.ndarray, tag: str = "") -> dict:
     if gpu_out.dtype == torch.float32:
         assert err.max() <= MAX_ABS, f"{tag}: max abs error {err.max():.3e} > {MAX_ABS}"
     else:
-        bound = np.maximum(MAX_ABS, bf16_ulp(r))
+        ulp = f16_ulp(r) if gpu_out.dtype == torch.float16 else bf16_ulp(r)
+        bound = np.maximum(MAX_ABS, ulp)
         bad = np.argwhere(err > bound)
         assert bad.size == 0, f"{tag}: {len(bad)} elements beyond max(2e-2, ulp); first {bad[:3].tolist()}"
     return stats
