@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = [
     "agmm_plan", "agmm_destroy", "agmm_workspace_bytes", "agmm_run", "agmm_run_unfused",
     "agmm_run_host", "agmm_query_status", "agmm_plan_info", "agmm_ring_chunks",
     "agmm_status_string", "agmm_last_error", "agmm_version", "agmm_trace_bytes", "agmm_set_trace",
-    "agmm_run_unfused_noalloc",
+    "agmm_run_unfused_noalloc", "agmm_run_gather",
 ]
 
 
@@ -76,6 +76,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.agmm_run.restype = c_int
     lib.agmm_run_unfused.argtypes = [vp, ctypes.POINTER(vp), vp, vp, c_int, vp, vp]
     lib.agmm_run_unfused.restype = c_int
+    lib.agmm_run_gather.argtypes = [vp, ctypes.POINTER(vp), vp, vp, vp, c_int, vp, vp]
+    lib.agmm_run_gather.restype = c_int
     lib.agmm_run_host.argtypes = [vp, ctypes.POINTER(vp), vp, vp, ctypes.POINTER(vp), vp, vp, c_int, vp, vp]
     lib.agmm_run_host.restype = c_int
     lib.agmm_query_status.argtypes = [vp, vp, vp]
@@ -217,6 +219,12 @@ class Plan:
                  stream_handle: Optional[int]) -> None:
         _check(self._lib.agmm_run(self._h, _ptr_array(x_ptrs), y_ptr, o_ptr, int(my_id), ws_ptr, stream_handle))
 
+    def run_gather(self, xs, y, o, xcat, my_id: int, workspace, stream=None) -> None:
+        """Fused path that also writes concat(xs) into xcat ([P*m, k], input dtype)."""
+        _check(self._lib.agmm_run_gather(self._h, _ptr_array([x.data_ptr() for x in xs]), y.data_ptr(),
+                                         o.data_ptr(), xcat.data_ptr(), int(my_id), workspace.data_ptr(),
+                                         _stream_handle(stream)))
+
     def run_unfused(self, xs, y, o, my_id: int, workspace, stream=None) -> None:
         """Gather into the workspace, then the same GEMM on the gathered buffer."""
         _check(self._lib.agmm_run_unfused(self._h, _ptr_array([x.data_ptr() for x in xs]), y.data_ptr(),
@@ -261,9 +269,10 @@ _plan_cache: Dict[tuple, Plan] = {}
 
 
 def all_gather_matmul(xs, y, my_id: int = 0, rhs_transpose: bool = False, out=None, unfused: bool = False,
-                      out_f32: bool = False, workspace=None, stream=None):
+                      out_f32: bool = False, workspace=None, stream=None, return_gathered: bool = False):
     """all-gather(xs, axis=0) @ y on one GPU; returns O [P*m, n] in the input
-    dtype (bf16 or fp16) or float32."""
+    dtype (bf16 or fp16) or float32.  With return_gathered it returns
+    (O, concat(xs)): the fused kernel stores the gathered rows as it loads them."""
     import torch
 
     m, k, n = _check_operands(xs, y, rhs_transpose)
@@ -277,5 +286,11 @@ def all_gather_matmul(xs, y, my_id: int = 0, rhs_transpose: bool = False, out=No
         out = torch.empty((plan.M, n), dtype=torch.float32 if out_f32 else xs[0].dtype, device=y.device)
     if workspace is None:
         workspace = plan.new_workspace(unfused, device=y.device)
+    if return_gathered:
+        if unfused:
+            raise ValueError("return_gathered uses the fused path")
+        xcat = torch.empty((plan.M, k), dtype=xs[0].dtype, device=y.device)
+        plan.run_gather(xs, y, out, xcat, my_id, workspace, stream)
+        return out, xcat
     (plan.run_unfused if unfused else plan.run)(xs, y, out, my_id, workspace, stream)
     return out

@@ -125,6 +125,7 @@ struct agmm_plan_s {
   bool cache_valid = false;
   const void* cache_x[kMaxShards] = {};
   const void* cache_y = nullptr;
+  const void* cache_xcat = nullptr;  // buffer the gathered-LHS maps describe
   KernelParams params{};
   agmm_plan_s* sub = nullptr;  // unfused path: P = 1 over the gathered buffer
   size_t out_elem = 2;
@@ -489,7 +490,22 @@ agmm_status_t check_run_args(agmm_plan_s* pl, const void* const* xs, const void*
 // status: the device status words; tail_ws: tail_bytes of workspace for the
 // split tail tiles (counters, then partials).
 agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y, void* o, int my_id,
-                           void* status, void* tail_ws, cudaStream_t stream) {
+                           void* status, void* tail_ws, cudaStream_t stream, void* xcat = nullptr) {
+  KernelParams& kpx = pl->params;
+  kpx.store_xcat = xcat != nullptr ? 1 : 0;
+  if (xcat != nullptr && xcat != pl->cache_xcat) {
+    // per-shard views of the gathered buffer: a store is clipped at its shard
+    std::string err;
+    for (int r = 0; r < pl->P; ++r) {
+      const void* base = static_cast<const uint8_t*>(xcat) + (size_t)r * pl->m_pd * pl->k * 2;
+      if (!encode_2d(&kpx.xcatmap[r], base, (uint64_t)pl->k, (uint64_t)pl->m_pd, kTileK, (uint32_t)pl->box_rows,
+                     pl->f16, &err)) {
+        pl->cache_xcat = nullptr;
+        return fail(AGMM_ERR_CUDA, "gathered-LHS tensor map: " + err);
+      }
+    }
+    pl->cache_xcat = xcat;
+  }
   bool same = pl->cache_valid && pl->cache_y == y;
   for (int r = 0; same && r < pl->P; ++r) same = pl->cache_x[r] == xs[r];
   KernelParams& kp = pl->params;
@@ -614,6 +630,26 @@ agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void
   if (st != AGMM_OK) return st;
   return launch_fused(plan, x_shards, y, o, my_id, workspace, static_cast<uint8_t*>(workspace) + kStatusBytes,
                       static_cast<cudaStream_t>(stream));
+}
+
+agmm_status_t agmm_run_gather(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o, void* xcat,
+                              int my_id, void* workspace, void* stream) {
+  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace);
+  if (st != AGMM_OK) return st;
+  if (!xcat) return fail(AGMM_ERR_INVALID_ARG, "xcat is NULL");
+  if (!aligned16(xcat)) return fail(AGMM_ERR_ALIGNMENT, "xcat must be 16-byte aligned");
+  if (plan->key.pair)
+    return fail(AGMM_ERR_UNSUPPORTED, "the CTA-pair row kernel does not store the gathered LHS (unset AGMM_PAIR)");
+  const size_t gbytes = (size_t)plan->M() * plan->k * 2;
+  const size_t xbytes = (size_t)plan->m_pd * plan->k * 2;
+  for (int r = 0; r < plan->P; ++r)
+    if (overlaps(x_shards[r], xbytes, xcat, gbytes)) return fail(AGMM_ERR_INVALID_ARG, "xcat overlaps a shard");
+  if (overlaps(y, (size_t)plan->k * plan->n * 2, xcat, gbytes) ||
+      overlaps(o, (size_t)plan->M() * plan->n * plan->out_elem, xcat, gbytes) ||
+      overlaps(workspace, agmm_workspace_bytes(plan, 0), xcat, gbytes))
+    return fail(AGMM_ERR_INVALID_ARG, "xcat overlaps Y, O or the workspace");
+  return launch_fused(plan, x_shards, y, o, my_id, workspace, static_cast<uint8_t*>(workspace) + kStatusBytes,
+                      static_cast<cudaStream_t>(stream), xcat);
 }
 
 agmm_status_t agmm_run_unfused(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o,

@@ -212,13 +212,19 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 
 // Two float32 values rounded (to nearest even) to the 16-bit output type:
 // bf16, or fp16 when f16.
+// Both conversions are computed and one is selected: no branch.
 __device__ __forceinline__ uint32_t pack_16x2(float lo, float hi, bool f16) {
-  if (f16) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  __half2 h = __floats2half2_rn(lo, hi);
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  const uint32_t hu = *reinterpret_cast<uint32_t*>(&h);
+  const uint32_t bu = *reinterpret_cast<uint32_t*>(&b);
+  return f16 ? hu : bu;
+}
+
+__device__ __forceinline__ uint16_t to_16(float v, bool f16) {
+  const uint16_t hu = __half_as_ushort(__float2half_rn(v));
+  const uint16_t bu = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return f16 ? hu : bu;
 }
 
 // Store 32 consecutive f32 accumulator values of one output row.
@@ -246,10 +252,8 @@ template <bool kF32>
 __device__ __forceinline__ void store_one(void* out, int64_t ldo, int64_t row, int64_t col, float v, bool f16) {
   if constexpr (kF32) {
     static_cast<float*>(out)[row * ldo + col] = v;
-  } else if (f16) {
-    static_cast<__half*>(out)[row * ldo + col] = __float2half_rn(v);
   } else {
-    static_cast<__nv_bfloat16*>(out)[row * ldo + col] = __float2bfloat16_rn(v);
+    static_cast<uint16_t*>(out)[row * ldo + col] = to_16(v, f16);
   }
 }
 
@@ -614,15 +618,32 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       uint64_t* wa = p.trace ? &waited_accfree : nullptr;
       SegmentIter iter;
       iter.init(p, cluster_id, nclusters);
+      const int cpt = kTileM / p.box_rows;
+      const uint32_t chunk_bytes = (uint32_t)p.box_rows * 128u;
+      bool stored_any = false;
       for (int tile = 0; ok; ++tile, ++it) {
         int kb0 = kb_begin, kb1 = kb_end;
+        // Gathered-LHS by-product: every CTA that loads an X box may store
+        // it, so each (X rows, k block) is stored by the one n tile whose
+        // share of the k range holds that k block: n tile t stores k blocks
+        // [t*K/T, (t+1)*K/T) of its range, and the stores are spread evenly.
+        bool store = false;
+        int st_mt = 0, st_lo = 0, st_hi = 0;
         if constexpr (kPath == kPathRows) {
           Segment sg;
           if (!iter.next(p, kCM, crank, sg)) break;
           kb0 = sg.kb0;
           kb1 = sg.kb1;
+          store = p.store_xcat && sg.mt < p.num_m_tiles;
+          st_mt = sg.mt;
+          st_lo = (int)((int64_t)sg.nt * p.num_k_blocks / p.num_n_tiles);
+          st_hi = (int)((int64_t)(sg.nt + 1) * p.num_k_blocks / p.num_n_tiles);
         } else {
           if (it > 0) break;
+          store = p.store_xcat != 0;
+          const int span = kb_end - kb_begin;
+          st_lo = kb_begin + (int)((int64_t)swap_nt * span / p.num_n_tiles);
+          st_hi = kb_begin + (int)((int64_t)(swap_nt + 1) * span / p.num_n_tiles);
         }
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
@@ -645,6 +666,28 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           if (it == 0 && kb == kb0) trace(p, 4);
           const uint32_t a_addr = a0 + (uint32_t)stage * kASlotBytes;
           const uint32_t b_addr = b0 + (uint32_t)stage * p.b_slot_bytes;
+          const bool store_kb = store && kb >= st_lo && kb < st_hi;
+          if (store_kb) {
+            // The landed X boxes go out to the gathered LHS as they are; the
+            // per-shard maps clip a box at its shard's last row.
+            if constexpr (kPath == kPathRows) {
+              for (int j = 0; j < cpt; ++j) {
+                const int64_t gc = (int64_t)st_mt * cpt + j;
+                if (gc < p.total_chunks) {
+                  const RingChunk ch = ring_chunk(geom, gc);
+                  ptx::tma_store_2d(&p.xcatmap[ch.shard], a_addr + (uint32_t)j * chunk_bytes, kb * kTileK,
+                                    (int)ch.src_row);
+                }
+              }
+            } else {
+              for (int c = 0; c < swap_nch; ++c) {
+                const int4 e = chunk_tab[swap_c0 + c];
+                ptx::tma_store_2d(&p.xcatmap[e.x], b_addr + (uint32_t)c * chunk_bytes, kb * kTileK, e.y);
+              }
+            }
+            ptx::bulk_commit();
+            stored_any = true;
+          }
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk) {
             // K-major operand: the 16-element k step moves 32 bytes inside the
@@ -660,6 +703,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             else
               ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
+          // the stores must have read the stage before it is released
+          if (store_kb) ptx::bulk_wait_read_all();
           // frees the stage (in every cluster CTA: their producers multicast
           // into it) once these MMAs finish
           if constexpr (kPair)
@@ -680,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         else
           ptx::mma_commit(bar_acc_full(ctl, acc));
       }
+      if (stored_any) ptx::bulk_wait_all();
       trace(p, 5);
       trace_value(p, 14, waited_full);
       trace_value(p, 15, waited_accfree);

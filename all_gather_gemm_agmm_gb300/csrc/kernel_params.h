@@ -72,6 +72,12 @@ struct __align__(128) KernelParams {
   int group_chunks;  // swap path: ring chunks per row group (blockIdx.z)
   int pdl;  // launched with programmatic stream serialization (host side only)
   int f16;  // X, Y and a 16-bit O are fp16 (else bf16)
+  // Optional by-product: the gathered LHS.  xcatmap[r] views rows
+  // [r*m_pd, (r+1)*m_pd) of the caller's [P*m_pd, k] buffer with the shard
+  // maps' box; with store_xcat each X box is stored there once, by the n
+  // tile whose share of the k range holds it.
+  CUtensorMap xcatmap[kMaxShards];
+  int store_xcat;
 };
 
 struct GatherParams {

@@ -103,6 +103,23 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* map, 
       : "memory");
 }
 
+// 2-D tiled store of one box from this CTA's shared memory (same swizzle as
+// the tensor map), tracked by the issuing thread's bulk groups.  The box is
+// clipped at the tensor's bounds.
+__device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(c0),
+               "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's committed bulk groups have finished reading
+// shared memory (the source may be overwritten afterwards).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until this thread's committed bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // The same box delivered to the same shared-memory offset (and the same
 // mbarrier offset) of every CTA of the cluster whose bit is set in cta_mask.
 __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* map, uint32_t bar, int c0,

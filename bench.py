@@ -343,6 +343,21 @@ def bench_ours(args, w):
     unf_ms = reduce_max(el2, device) / K2 * 1e3
     del g2
 
+    # the fused path that also writes the gathered LHS (what the unfused path
+    # materialises too): one gathered buffer per replica, same method
+    # (the opt-in CTA-pair row kernel does not store it: no entry then)
+    gath_ms = None
+    if os.environ.get("AGMM_PAIR", "0") in ("", "0"):
+        xcats = [torch.empty((w.M, w.k), dtype=r[2].dtype, device=device) for r in reps]
+        torch.cuda.synchronize()
+        gath = [(lambda rep, xc: (lambda s: plan.run_gather(rep[0], rep[1], rep[2], xc, w.my_id, ws, s)))(r, xc)
+                for r, xc in zip(reps, xcats)]
+        g3 = time_graph(gath, K, args.warmup, stream)
+        el3, _ = run_timed(g3, gath, K2, stream)
+        plan.query_status(ws, stream)
+        gath_ms = reduce_max(el3, device) / K2 * 1e3
+        del g3, xcats
+
     # end to end through the C ABI from pinned host memory.  Two steps are in
     # flight: each slot has its own device buffers, plan, workspace and
     # stream, so one step's uploads overlap the previous step's kernel and
@@ -424,6 +439,9 @@ def bench_ours(args, w):
         "roofline": roof,
         "unfused": {"ms_per_step": unf_ms, "value": w.flops / (unf_ms / 1e3) / 1e12 * ws_n, "steps": K2,
                     "fused_speedup": unf_ms / ms_per_step},
+        "with_gathered": None if gath_ms is None else {
+            "ms_per_step": gath_ms, "steps": K2, "vs_unfused": unf_ms / gath_ms,
+            "cost_over_fused": gath_ms / ms_per_step},
         "e2e": e2e,
         "gpu_launches": K,
         "clocks": clocks,

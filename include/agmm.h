@@ -139,6 +139,28 @@ agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void
                        int my_id, void* workspace, void* stream);
 
 /*
+ * agmm_run_gather -- agmm_run that also writes the gathered left-hand side.
+ *
+ * Source: tpu_inference "all_gather_matmul.py", the module's note on
+ * splitting a large n (one all-gather matmul returns its output block and
+ * the gathered x; the next block is then a plain matmul of that x), and the
+ * kernel's x scratch output, which holds the shards a device received.
+ *
+ * Same arguments and result as agmm_run, plus
+ *   xcat  device pointer to [P*m_per_device, k] elements of the input type,
+ *         row-major, 16-byte aligned, caller-owned; on return (stream order)
+ *         it holds concat(X_0, ..., X_{P-1}) in rank order, bit for bit.
+ * Each X box is stored straight from shared memory (TMA) by one of the CTAs
+ * that load it: n tile t stores the k blocks in the t-th share of the k
+ * range, so the gathered rows are written once, never read back, and the
+ * store work is spread over all n tiles.  xcat must not overlap the shards, Y, O or the workspace
+ * (AGMM_ERR_INVALID_ARG).  Plans of the opt-in CTA-pair row kernel
+ * (AGMM_PAIR=1) return AGMM_ERR_UNSUPPORTED.
+ */
+agmm_status_t agmm_run_gather(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o, void* xcat,
+                              int my_id, void* workspace, void* stream);
+
+/*
  * agmm_run_unfused -- the decomposed comparison path: a gather kernel copies
  * shard r to rows [r*m_per_device, (r+1)*m_per_device) of a scratch buffer in
  * the workspace (the decomposed approach of the AllGather-GEMM tutorial), then

@@ -60,6 +60,7 @@ def test_plan_rejects_bad_shapes_before_cuda(agmm_lib, args, why):
 
 def test_plan_rejects_bad_dtype_and_flag(agmm_lib):
     assert _plan(agmm_lib, 2, 16, 256, 128, dtype=7)[0] == agmm.AGMM_ERR_INVALID_ARG
+    assert _plan(agmm_lib, 2, 16, 256, 128, dtype=-1)[0] == agmm.AGMM_ERR_INVALID_ARG
     assert _plan(agmm_lib, 2, 16, 256, 128, rt=2)[0] == agmm.AGMM_ERR_INVALID_ARG
     assert agmm_lib.agmm_plan(2, 16, 256, 128, 0, 0, None) == agmm.AGMM_ERR_INVALID_ARG
 
@@ -70,6 +71,7 @@ def test_null_plan_calls(agmm_lib):
     arr = (ctypes.c_void_p * 1)()
     assert agmm_lib.agmm_run(None, arr, None, None, 0, None, None) == agmm.AGMM_ERR_INVALID_ARG
     assert agmm_lib.agmm_run_unfused(None, arr, None, None, 0, None, None) == agmm.AGMM_ERR_INVALID_ARG
+    assert agmm_lib.agmm_run_gather(None, arr, None, None, None, 0, None, None) == agmm.AGMM_ERR_INVALID_ARG
     assert agmm_lib.agmm_plan_info(None, None) == agmm.AGMM_ERR_INVALID_ARG
     assert agmm_lib.agmm_query_status(None, None, None) == agmm.AGMM_ERR_INVALID_ARG
 
