@@ -9,7 +9,9 @@
 //               per-shard tensor-map table, in ring order) and Y tiles into a
 //               multi-stage shared-memory ring guarded by full/empty mbarriers;
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma
-//               (bf16 x bf16 -> f32 accumulators in TMEM) and tcgen05.commit;
+//               (bf16 x bf16 or fp16 x fp16 -> f32 accumulators in TMEM) and
+//               tcgen05.commit; optionally it also TMA-stores the landed X
+//               boxes to a gathered-LHS buffer before releasing each stage;
 //   warps 2-5   drain TMEM with tcgen05.ld, round to the output dtype and store
 //               each row at its rank-order offset.
 //
@@ -18,11 +20,11 @@
 //              persistent CTAs walk the tile list, TMEM holds two accumulators
 //              so the epilogue of one tile overlaps the main loop of the next.
 //   swap path  (the whole gathered LHS fits in one MMA N <= 256) MMA M = 128
-//              columns of n, MMA N = every gathered row; k is split across the
-//              CTAs of a thread-block cluster and the float32 partials are
-//              summed in a fixed rank order (through an L2-resident
-//              workspace, or distributed shared memory), so Y is read from
-//              device memory once per row group of the gathered rows.
+//              columns of n, MMA N = the gathered rows of one row group; k is
+//              split across the CTAs of a thread-block cluster and the float32
+//              partials are summed in a fixed rank order (through an
+//              L2-resident workspace, or distributed shared memory), so each
+//              byte of Y comes from device memory once.
 //
 // Every mbarrier wait is bounded (KernelParams::wait_limit_cycles).  A wait that
 // runs out raises a shared abort flag and records AGMM_ERR_TIMEOUT in the

@@ -114,7 +114,7 @@ void agmm_destroy(agmm_plan_t plan);
 /*
  * Bytes of device workspace agmm_run (unfused == 0) or agmm_run_unfused
  * (unfused != 0) needs.  The first 256 bytes hold the device status words;
- * the unfused path adds the gathered [P*m_per_device, k] bf16 buffer at
+ * the unfused path adds the gathered [P*m_per_device, k] buffer (input type) at
  * offset 256.  The workspace must be zero-filled before its first use and
  * must not be shared by runs that overlap on the device.  Returns 0 for NULL.
  */
