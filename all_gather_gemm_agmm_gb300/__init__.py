@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = [
     "agmm_plan", "agmm_destroy", "agmm_workspace_bytes", "agmm_run", "agmm_run_unfused",
     "agmm_run_host", "agmm_query_status", "agmm_plan_info", "agmm_ring_chunks",
     "agmm_status_string", "agmm_last_error", "agmm_version", "agmm_trace_bytes", "agmm_set_trace",
-    "agmm_run_unfused_noalloc", "agmm_run_gather",
+    "agmm_run_unfused_noalloc", "agmm_run_gather", "agmm_plan_preview",
 ]
 
 
@@ -78,6 +78,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.agmm_run_unfused.restype = c_int
     lib.agmm_run_gather.argtypes = [vp, ctypes.POINTER(vp), vp, vp, vp, c_int, vp, vp]
     lib.agmm_run_gather.restype = c_int
+    lib.agmm_plan_preview.argtypes = [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, c_int, c_int, c_int,
+                                      ctypes.POINTER(PlanInfo)]
+    lib.agmm_plan_preview.restype = c_int
     lib.agmm_run_host.argtypes = [vp, ctypes.POINTER(vp), vp, vp, ctypes.POINTER(vp), vp, vp, c_int, vp, vp]
     lib.agmm_run_host.restype = c_int
     lib.agmm_query_status.argtypes = [vp, vp, vp]
@@ -144,6 +147,21 @@ def ring_chunks(P: int, m_per_device: int, my_id: int, box_rows: int, whole_shar
     valid = (ctypes.c_int32 * cnt)()
     _check(lib.agmm_ring_chunks(P, m_per_device, my_id, box_rows, w, shard, src, out, valid, cnt, ctypes.byref(n)))
     return {"shard": list(shard), "src_row": list(src), "out_row": list(out), "valid": list(valid)}
+
+
+def plan_preview(P: int, m_per_device: int, k: int, n: int, rhs_transpose: bool = False, num_sms: int = 152,
+                 out_f32: bool = False, f16: bool = False) -> Dict[str, int]:
+    """The tile choice for a device with ``num_sms`` SMs, computed on the host
+    without CUDA (see agmm_plan_preview in agmm.h)."""
+    lib = load_library()
+    if f16:
+        dtype = AGMM_F16_F32OUT if out_f32 else AGMM_F16
+    else:
+        dtype = AGMM_BF16_F32OUT if out_f32 else AGMM_BF16
+    inf = PlanInfo()
+    _check(lib.agmm_plan_preview(int(P), int(m_per_device), int(k), int(n), dtype, int(bool(rhs_transpose)),
+                                 int(num_sms), ctypes.byref(inf)))
+    return {f: getattr(inf, f) for f, _ in PlanInfo._fields_}
 
 
 class Plan:

@@ -758,6 +758,45 @@ agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info) {
   return AGMM_OK;
 }
 
+agmm_status_t agmm_plan_preview(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
+                                int rhs_transpose, int num_sms, agmm_plan_info_t* info) {
+  if (!info) return fail(AGMM_ERR_INVALID_ARG, "info is NULL");
+  if (num_sms < 1 || num_sms > 4096) return fail(AGMM_ERR_INVALID_ARG, "num_sms must be in [1, 4096]");
+  agmm_status_t st = validate_shape(P, m_per_device, k, n, (int)dtype, rhs_transpose);
+  if (st != AGMM_OK) return st;
+  agmm_plan_s pl;
+  pl.P = P;
+  pl.m_pd = m_per_device;
+  pl.k = k;
+  pl.n = n;
+  pl.dtype = dtype;
+  pl.rhs_t = rhs_transpose;
+  pl.num_sms = num_sms;
+  pl.key.y_kmajor = rhs_transpose != 0;
+  pl.key.out_f32 = dtype == AGMM_BF16_F32OUT || dtype == AGMM_F16_F32OUT;
+  pl.f16 = dtype == AGMM_F16 || dtype == AGMM_F16_F32OUT;
+  st = choose_tiles(&pl);
+  if (st != AGMM_OK) return st;
+  info->path = pl.key.path;
+  info->box_rows = pl.box_rows;
+  info->whole_shards = pl.whole_shards;
+  info->chunks = pl.total_chunks;
+  info->tile_m = kTileM;
+  info->tile_n = pl.mma_n;
+  info->tile_k = kTileK;
+  info->stages = pl.stages;
+  info->splits = pl.splits;
+  info->num_tiles = pl.num_tiles;
+  const int cm = pl.key.path == kPathSwap ? 1 : pl.key.cm;
+  info->num_ctas = pl.key.path == kPathSwap ? pl.splits * pl.num_n_tiles * pl.row_groups
+                                            : std::min(pl.num_tiles * cm, (num_sms / cm) * cm);
+  info->group_m = pl.group_m;
+  info->num_sms = num_sms;
+  info->smem_bytes = pl.smem_bytes;
+  info->row_groups = pl.key.path == kPathSwap ? pl.row_groups : 1;
+  return AGMM_OK;
+}
+
 agmm_status_t agmm_ring_chunks(int P, int64_t m_per_device, int my_id, int box_rows, int whole_shards,
                                int32_t* shard, int64_t* src_row, int64_t* out_row, int32_t* valid,
                                int64_t max_chunks, int64_t* n_chunks) {

@@ -234,6 +234,19 @@ agmm_status_t agmm_set_trace(agmm_plan_t plan, void* trace, size_t bytes);
 agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info);
 
 /*
+ * agmm_plan_preview -- the tile choice agmm_plan would start from on a device
+ * with num_sms SMs, computed on the host alone: no CUDA call, so it works
+ * without a GPU (tests, tooling).  Same shape arguments and validation as
+ * agmm_plan.  The device-dependent steps that agmm_plan adds afterwards are
+ * absent: lowering the k splits until every cluster is resident, and
+ * sizing the row path's persistent grid.  So `splits` is an upper bound and
+ * `num_ctas` is the grid before them.  Returns AGMM_ERR_INVALID_ARG for a
+ * NULL info or num_sms outside [1, 4096].
+ */
+agmm_status_t agmm_plan_preview(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
+                                int rhs_transpose, int num_sms, agmm_plan_info_t* info);
+
+/*
  * The ring-ordered row sequence, host side (no device needed).  For box
  * height box_rows the sequence is cut into chunks; chunk c covers rows
  * [src_row[c], src_row[c] + valid[c]) of shard shard[c], which land at rows
