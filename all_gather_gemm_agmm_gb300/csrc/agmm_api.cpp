@@ -153,6 +153,18 @@ agmm_status_t validate_shape(int P, int64_t m_pd, int64_t k, int64_t n, int dtyp
   return AGMM_OK;
 }
 
+// tcgen05.alloc blocks until the SM has the columns free, so the CTAs that
+// shared memory lets share an SM must fit in its 512 TMEM columns together;
+// otherwise a CTA could wait on a CTA of another cluster that waits on it.
+// Pads the request so that at most 512 / tmem_cols CTAs are resident per SM
+// (228 KiB of shared memory per SM, 1 KiB of it reserved per CTA).
+size_t tmem_safe_smem(size_t smem, int tmem_cols) {
+  constexpr size_t kSmemPerSm = 233472;
+  const size_t fit = (size_t)(512 / std::max(32, tmem_cols));
+  const size_t floor_bytes = kSmemPerSm / (fit + 1) + 1;  // fit + 1 CTAs would not fit
+  return std::min(kMaxDynSmem, std::max(smem, floor_bytes));
+}
+
 // Tile planning for a device with `num_sms` SMs (pure host logic).
 agmm_status_t choose_tiles(agmm_plan_s* pl) {
   const int force_path = env_int("AGMM_PATH", -1);
@@ -298,7 +310,8 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->tmem_cols = 2 * bn;
     pl->group_m = std::max(1, env_int("AGMM_GROUP_M", 8));
   }
-  pl->smem_bytes = 1024 + (size_t)pl->stages * (kASlotBytes + pl->b_slot_bytes) + kCtlBytes;
+  pl->smem_bytes = tmem_safe_smem(1024 + (size_t)pl->stages * (kASlotBytes + pl->b_slot_bytes) + kCtlBytes,
+                                  pl->tmem_cols);
   return AGMM_OK;
 }
 
@@ -367,7 +380,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
         --pl->splits;
         continue;
       }
-      pl->smem_bytes = 1024 + (size_t)pl->stages * stage_bytes + kCtlBytes;
+      pl->smem_bytes = tmem_safe_smem(1024 + (size_t)pl->stages * stage_bytes + kCtlBytes, pl->tmem_cols);
     }
     int active = 0;
     const int cluster = pl->key.path == kPathSwap ? pl->splits : pl->key.cm;

@@ -115,3 +115,29 @@ def test_preview_argument_errors():
     assert lib.agmm_plan_preview(2, 16, 200, 128, 0, 0, 152, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
     assert lib.agmm_plan_preview(9, 16, 256, 128, 0, 0, 152, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
     assert lib.agmm_plan_preview(2, 16, 256, 128, 5, 0, 152, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
+
+
+def _tmem_cols(info):
+    if info["path"] == 0:
+        return 2 * info["tile_n"]  # two accumulators of tile_n columns
+    c = 32
+    while c < info["tile_n"]:
+        c *= 2
+    return c
+
+
+@pytest.mark.parametrize("stages", ["2", "3", "8"])
+def test_resident_ctas_fit_tensor_memory(stages, monkeypatch):
+    # tcgen05.alloc waits for free columns: the CTAs that fit on one SM by
+    # shared memory (228 KiB, 1 KiB reserved per CTA) must fit in its 512
+    # TMEM columns together, even when fewer pipeline stages shrink a CTA
+    monkeypatch.setenv("AGMM_STAGES", stages)
+    rng = np.random.default_rng(7)
+    for _ in range(150):
+        P = int(rng.integers(1, 9))
+        m = int(rng.choice([1, 8, 16, 64, 128, 300, 2048]))
+        k = 128 * int(rng.integers(1, 40))
+        n = 256 * int(rng.integers(1, 20))
+        info = agmm.plan_preview(P, m, k, n, bool(rng.integers(0, 2)), num_sms=SMS)
+        resident = 233472 // (info["smem_bytes"] + 1024)
+        assert 1 <= resident and resident * _tmem_cols(info) <= 512, (P, m, k, n, info)
