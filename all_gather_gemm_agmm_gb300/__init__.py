@@ -34,8 +34,18 @@ EXPORTED_SYMBOLS = [
     "agmm_plan", "agmm_destroy", "agmm_workspace_bytes", "agmm_run", "agmm_run_unfused",
     "agmm_run_host", "agmm_query_status", "agmm_plan_info", "agmm_ring_chunks",
     "agmm_status_string", "agmm_last_error", "agmm_version", "agmm_trace_bytes", "agmm_set_trace",
-    "agmm_run_unfused_noalloc", "agmm_run_gather", "agmm_plan_preview",
+    "agmm_run_unfused_noalloc", "agmm_run_gather", "agmm_plan_preview", "agmm_plan_config",
 ]
+
+# agmm_tile_config_t: 0 leaves a field to the planner (the tuned table, else
+# its rules); on/off fields take AGMM_CFG_OFF / AGMM_CFG_ON.
+AGMM_CFG_AUTO = 0
+AGMM_CFG_OFF = 1
+AGMM_CFG_ON = 2
+CONFIG_FIELDS = ("path", "chunks", "box_rows", "tile_n", "cluster_m", "cta_pair", "stages", "group_m",
+                 "stream_k", "row_groups", "splits", "dsmem_reduce", "tuned_table")
+_ON_OFF = ("cta_pair", "stream_k", "dsmem_reduce", "tuned_table")
+_NAMED = {"path": {"rows": 1, "swap": 2}, "chunks": {"half": 1, "whole": 2}}
 
 
 class AgmmError(RuntimeError):
@@ -50,8 +60,54 @@ class PlanInfo(ctypes.Structure):
         ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int),
         ("stages", ctypes.c_int), ("splits", ctypes.c_int), ("num_tiles", ctypes.c_int),
         ("num_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("num_sms", ctypes.c_int),
-        ("smem_bytes", ctypes.c_size_t), ("row_groups", ctypes.c_int),
+        ("smem_bytes", ctypes.c_size_t), ("row_groups", ctypes.c_int), ("cluster_m", ctypes.c_int),
+        ("cta_pair", ctypes.c_int), ("stream_k_tiles", ctypes.c_int), ("dsmem_reduce", ctypes.c_int),
+        ("config_source", ctypes.c_int),
     ]
+
+
+class TileConfig(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int) for f in CONFIG_FIELDS]
+
+
+def tile_config(config: Optional[Dict[str, object]]) -> Optional[TileConfig]:
+    """A TileConfig from a dict of agmm_tile_config_t fields (None: no config).
+
+    ``path`` takes "rows" / "swap" (or 1 / 2), ``chunks`` "half" / "whole" (or
+    1 / 2); on/off fields (cta_pair, stream_k, dsmem_reduce, tuned_table) take
+    booleans; the rest are integers.  Missing or None fields stay 0, the
+    planner's choice."""
+    if config is None:
+        return None
+    unknown = set(config) - set(CONFIG_FIELDS)
+    if unknown:
+        raise ValueError(f"unknown tile config fields: {sorted(unknown)}")
+    tc = TileConfig()
+    for f, v in config.items():
+        if v is None:
+            continue
+        if f in _ON_OFF and isinstance(v, bool):
+            v = AGMM_CFG_ON if v else AGMM_CFG_OFF
+        elif f in _NAMED and isinstance(v, str):
+            v = _NAMED[f][v]
+        setattr(tc, f, int(v))
+    return tc
+
+
+def config_dict(tc: TileConfig) -> Dict[str, object]:
+    """The set fields of a TileConfig, in tile_config's notation."""
+    out: Dict[str, object] = {}
+    for f in CONFIG_FIELDS:
+        v = getattr(tc, f)
+        if v == 0:
+            continue
+        if f in _ON_OFF:
+            out[f] = v == AGMM_CFG_ON
+        elif f in _NAMED:
+            out[f] = {b: a for a, b in _NAMED[f].items()}.get(v, v)
+        else:
+            out[f] = v
+    return out
 
 
 _lib = None
@@ -78,8 +134,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.agmm_run_unfused.restype = c_int
     lib.agmm_run_gather.argtypes = [vp, ctypes.POINTER(vp), vp, vp, vp, c_int, vp, vp]
     lib.agmm_run_gather.restype = c_int
-    lib.agmm_plan_preview.argtypes = [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, c_int, c_int, c_int,
-                                      ctypes.POINTER(PlanInfo)]
+    lib.agmm_plan_preview.argtypes = [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, c_int, c_int,
+                                      ctypes.POINTER(TileConfig), c_int, ctypes.POINTER(PlanInfo)]
+    lib.agmm_plan_config.argtypes = [c_int, i64, i64, i64, c_int, c_int, ctypes.POINTER(TileConfig),
+                                     ctypes.POINTER(vp)]
+    lib.agmm_plan_config.restype = c_int
     lib.agmm_plan_preview.restype = c_int
     lib.agmm_run_host.argtypes = [vp, ctypes.POINTER(vp), vp, vp, ctypes.POINTER(vp), vp, vp, c_int, vp, vp]
     lib.agmm_run_host.restype = c_int
@@ -150,25 +209,31 @@ def ring_chunks(P: int, m_per_device: int, my_id: int, box_rows: int, whole_shar
 
 
 def plan_preview(P: int, m_per_device: int, k: int, n: int, rhs_transpose: bool = False, num_sms: int = 152,
-                 out_f32: bool = False, f16: bool = False) -> Dict[str, int]:
+                 out_f32: bool = False, f16: bool = False,
+                 config: Optional[Dict[str, object]] = None) -> Dict[str, int]:
     """The tile choice for a device with ``num_sms`` SMs, computed on the host
-    without CUDA (see agmm_plan_preview in agmm.h)."""
+    without CUDA (see agmm_plan_preview in agmm.h); ``config`` as for Plan."""
     lib = load_library()
     if f16:
         dtype = AGMM_F16_F32OUT if out_f32 else AGMM_F16
     else:
         dtype = AGMM_BF16_F32OUT if out_f32 else AGMM_BF16
     inf = PlanInfo()
+    tc = tile_config(config)
     _check(lib.agmm_plan_preview(int(P), int(m_per_device), int(k), int(n), dtype, int(bool(rhs_transpose)),
-                                 int(num_sms), ctypes.byref(inf)))
+                                 ctypes.byref(tc) if tc is not None else None, int(num_sms), ctypes.byref(inf)))
     return {f: getattr(inf, f) for f, _ in PlanInfo._fields_}
 
 
 class Plan:
-    """A planned problem: P shards of [m_per_device, k] times Y ([k, n] or [n, k])."""
+    """A planned problem: P shards of [m_per_device, k] times Y ([k, n] or [n, k]).
+
+    ``config`` (a dict, see tile_config) fixes tile choices; fields it leaves
+    out come from the tuned table for this exact shape, else the planner's
+    rules."""
 
     def __init__(self, P: int, m_per_device: int, k: int, n: int, rhs_transpose: bool = False,
-                 out_f32: bool = False, f16: bool = False):
+                 out_f32: bool = False, f16: bool = False, config: Optional[Dict[str, object]] = None):
         self._lib = load_library()
         self.P, self.m_per_device, self.k, self.n = int(P), int(m_per_device), int(k), int(n)
         self.rhs_transpose = bool(rhs_transpose)
@@ -179,8 +244,10 @@ class Plan:
         else:
             dtype = AGMM_BF16_F32OUT if out_f32 else AGMM_BF16
         h = ctypes.c_void_p()
-        _check(self._lib.agmm_plan(self.P, self.m_per_device, self.k, self.n, dtype, int(self.rhs_transpose),
-                                   ctypes.byref(h)))
+        tc = tile_config(config)
+        _check(self._lib.agmm_plan_config(self.P, self.m_per_device, self.k, self.n, dtype,
+                                          int(self.rhs_transpose), ctypes.byref(tc) if tc is not None else None,
+                                          ctypes.byref(h)))
         self._h = h
 
     @property

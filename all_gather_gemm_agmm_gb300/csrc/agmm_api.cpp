@@ -120,6 +120,8 @@ struct agmm_plan_s {
   bool f16 = false;         // fp16 operands (else bf16)
   int clock_khz = 2100000;  // peak SM clock of the planned device
   int group_chunks = 0;     // swap path: ring chunks per row group
+  bool stream_k = true;     // rows path: share a ragged last wave's k blocks
+  int config_source = 0;    // agmm_plan_info_t::config_source
   size_t tail_bytes = 0;  // workspace bytes for tail counters and partials
   // descriptor cache: tensor maps depend only on the X and Y pointers
   bool cache_valid = false;
@@ -165,36 +167,167 @@ size_t tmem_safe_smem(size_t smem, int tmem_cols) {
   return std::min(kMaxDynSmem, std::max(smem, floor_bytes));
 }
 
-// Tile planning for a device with `num_sms` SMs (pure host logic).
-agmm_status_t choose_tiles(agmm_plan_s* pl) {
-  const int force_path = env_int("AGMM_PATH", -1);
-  // AGMM_CHUNKS=half|whole restricts the chunking mode (tests, tuning).
-  const char* force_chunks = std::getenv("AGMM_CHUNKS");
-  const int whole_lo = (force_chunks && std::strcmp(force_chunks, "whole") == 0) ? 1 : 0;
-  const int whole_hi = (force_chunks && std::strcmp(force_chunks, "half") == 0) ? 0 : 1;
+// The tuned table: measured tile configurations for exact shapes, written by
+// the package's tuner (tune.py) from its timing runs on GB300.
+struct TunedEntry {
+  int P;
+  int64_t m_pd, k, n;
+  int rhs_t, f16;
+  agmm_tile_config_t cfg;
+};
+const TunedEntry kTunedTable[] = {
+#include "tuned_sm103.inc"
+    {0, 0, 0, 0, 0, 0, {}}  // end marker
+};
+
+const agmm_tile_config_t* tuned_lookup(int P, int64_t m_pd, int64_t k, int64_t n, int rhs_t, bool f16) {
+  for (const TunedEntry& e : kTunedTable)
+    if (e.P == P && e.m_pd == m_pd && e.k == k && e.n == n && e.rhs_t == rhs_t && e.f16 == (f16 ? 1 : 0))
+      return &e.cfg;
+  return nullptr;
+}
+
+bool on_off_ok(int v) { return v == AGMM_CFG_AUTO || v == AGMM_CFG_OFF || v == AGMM_CFG_ON; }
+
+agmm_status_t validate_config(const agmm_tile_config_t* c) {
+  if (!c) return AGMM_OK;
+  const bool box_ok = c->box_rows == 0 || c->box_rows == 8 || c->box_rows == 16 || c->box_rows == 32 ||
+                      c->box_rows == 64 || c->box_rows == 128;
+  const bool rg_ok = c->row_groups == 0 || (c->row_groups >= 1 && c->row_groups <= 256 &&
+                                            (c->row_groups & (c->row_groups - 1)) == 0);
+  if (c->path < 0 || c->path > 2) return fail(AGMM_ERR_INVALID_ARG, "config.path must be 0, 1 or 2");
+  if (c->chunks < 0 || c->chunks > 2) return fail(AGMM_ERR_INVALID_ARG, "config.chunks must be 0, 1 or 2");
+  if (!box_ok) return fail(AGMM_ERR_INVALID_ARG, "config.box_rows must be 0, 8, 16, 32, 64 or 128");
+  if (c->tile_n != 0 && c->tile_n != 128 && c->tile_n != 256)
+    return fail(AGMM_ERR_INVALID_ARG, "config.tile_n must be 0, 128 or 256");
+  if (c->cluster_m < 0 || c->cluster_m > 2) return fail(AGMM_ERR_INVALID_ARG, "config.cluster_m must be 0, 1 or 2");
+  if (!on_off_ok(c->cta_pair) || !on_off_ok(c->stream_k) || !on_off_ok(c->dsmem_reduce) ||
+      !on_off_ok(c->tuned_table))
+    return fail(AGMM_ERR_INVALID_ARG, "on/off config fields take AGMM_CFG_AUTO, AGMM_CFG_OFF or AGMM_CFG_ON");
+  if (c->stages != 0 && (c->stages < 2 || c->stages > kMaxStages))
+    return fail(AGMM_ERR_INVALID_ARG, "config.stages must be 0 or in [2, 8]");
+  if (c->group_m < 0 || c->group_m > 65536) return fail(AGMM_ERR_INVALID_ARG, "config.group_m must be in [0, 65536]");
+  if (!rg_ok) return fail(AGMM_ERR_INVALID_ARG, "config.row_groups must be 0 or a power of two up to 256");
+  if (c->splits < 0 || c->splits > 16) return fail(AGMM_ERR_INVALID_ARG, "config.splits must be in [0, 16]");
+  return AGMM_OK;
+}
+
+// AGMM_* environment overrides (tests and experiments) as a config; values
+// out of range are ignored.
+agmm_tile_config_t env_config() {
+  agmm_tile_config_t c{};
+  auto on_off = [](const char* name) {
+    const char* v = std::getenv(name);
+    if (!v || !*v) return AGMM_CFG_AUTO;
+    return std::atoi(v) != 0 ? AGMM_CFG_ON : AGMM_CFG_OFF;
+  };
+  const int path = env_int("AGMM_PATH", -1);  // 0: row tiles, 1: swapped tiles
+  if (path == kPathRows || path == kPathSwap) c.path = path == kPathRows ? 1 : 2;
+  const char* ch = std::getenv("AGMM_CHUNKS");  // half | whole
+  if (ch && std::strcmp(ch, "half") == 0) c.chunks = 1;
+  if (ch && std::strcmp(ch, "whole") == 0) c.chunks = 2;
+  const int bn = env_int("AGMM_BN", 0);
+  if (bn == 128 || bn == 256) c.tile_n = bn;
+  const int cm = env_int("AGMM_CM", 0);
+  if (cm == 1 || cm == 2) c.cluster_m = cm;
+  c.cta_pair = on_off("AGMM_PAIR");
+  const int st = env_int("AGMM_STAGES", 0);
+  if (st >= 1) c.stages = std::min(kMaxStages, std::max(2, st));
+  const int gm = env_int("AGMM_GROUP_M", 0);
+  if (gm >= 1) c.group_m = std::min(gm, 65536);
+  c.stream_k = on_off("AGMM_STREAMK");
+  const int rg = env_int("AGMM_ROWGROUPS", 0);
+  if (rg >= 1) c.row_groups = rg;
+  const int sk = env_int("AGMM_SPLITK", 0);
+  if (sk >= 1) c.splits = std::min(sk, 16);
+  c.dsmem_reduce = on_off("AGMM_SWAP_DSMEM");
+  c.tuned_table = on_off("AGMM_TUNED");
+  return c;
+}
+
+bool any_tile_field(const agmm_tile_config_t& c) {
+  return c.path || c.chunks || c.box_rows || c.tile_n || c.cluster_m || c.cta_pair || c.stages || c.group_m ||
+         c.stream_k || c.row_groups || c.splits || c.dsmem_reduce;
+}
+
+// Fields of `top` that are set replace those of `base`.
+void overlay(agmm_tile_config_t* base, const agmm_tile_config_t& top) {
+  auto pick = [](int& b, int t) {
+    if (t != 0) b = t;
+  };
+  pick(base->path, top.path);
+  pick(base->chunks, top.chunks);
+  pick(base->box_rows, top.box_rows);
+  pick(base->tile_n, top.tile_n);
+  pick(base->cluster_m, top.cluster_m);
+  pick(base->cta_pair, top.cta_pair);
+  pick(base->stages, top.stages);
+  pick(base->group_m, top.group_m);
+  pick(base->stream_k, top.stream_k);
+  pick(base->row_groups, top.row_groups);
+  pick(base->splits, top.splits);
+  pick(base->dsmem_reduce, top.dsmem_reduce);
+  pick(base->tuned_table, top.tuned_table);
+}
+
+// The configuration a plan is built from: the caller's set fields, then the
+// environment's, then the tuned table's entry for the exact shape.  Fields
+// the caller set are strict (an infeasible one fails the plan); the others
+// fall back to the planner's rules when they cannot hold.
+struct ResolvedConfig {
+  agmm_tile_config_t cfg{};
+  agmm_tile_config_t strict{};
+  int source = 0;
+};
+
+ResolvedConfig resolve_config(const agmm_plan_s* pl, const agmm_tile_config_t* user) {
+  ResolvedConfig r;
+  const agmm_tile_config_t env = env_config();
+  if (user) r.strict = *user;
+  const int table_switch = user && user->tuned_table ? user->tuned_table : env.tuned_table;
+  const agmm_tile_config_t* tuned =
+      table_switch == AGMM_CFG_OFF ? nullptr : tuned_lookup(pl->P, pl->m_pd, pl->k, pl->n, pl->rhs_t, pl->f16);
+  if (tuned) {
+    r.cfg = *tuned;
+    r.source = 1;
+  }
+  overlay(&r.cfg, env);
+  overlay(&r.cfg, r.strict);
+  if (any_tile_field(env) || any_tile_field(r.strict)) r.source = 2;
+  return r;
+}
+
+// Tile planning for a device with `num_sms` SMs (pure host logic), from the
+// resolved configuration `c`; fields of `strict` that are set must hold.
+agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const agmm_tile_config_t& strict) {
+  const int whole_lo = c.chunks == 2 ? 1 : 0;
+  const int whole_hi = c.chunks == 1 ? 0 : 1;
+  const int bh_top = c.box_rows ? c.box_rows : 128;
+  const int bh_bottom = c.box_rows ? c.box_rows : 8;
   // Swap path: the whole ring-ordered row sequence (chunks padded to their box
   // height) fits in one MMA N of at most 256.  Candidates: half-shard chunks
   // (the ring's half split) or whole-shard chunks, each with box heights 8..128.
   // Cost: padded rows (MMA N, reduction volume) plus 16 rows per chunk (one
   // TMA box per chunk and stage).  Ties keep the half split and larger boxes.
   int best_bh = -1, best_whole = 0;
-  int64_t best_pad = 0, best_cost = 0;
+  int64_t best_cost = 0;
   for (int whole = whole_lo; whole <= whole_hi; ++whole) {
-    for (int bh = 128; bh >= 8; bh >>= 1) {
+    for (int bh = bh_top; bh >= bh_bottom; bh >>= 1) {
       const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh, whole);
       const int64_t pad = ring_padded_rows(g);
       const int64_t cost = pad + 16 * ring_total_chunks(g);
       if (pad <= 256 && (best_bh < 0 || cost < best_cost)) {
         best_bh = bh;
         best_whole = whole;
-        best_pad = pad;
         best_cost = cost;
       }
     }
   }
+  if (best_bh < 0 && strict.path == 2)
+    return fail(AGMM_ERR_UNSUPPORTED, "swapped tiles need the gathered rows, padded to box heights, within 256");
   const int64_t budget = (int64_t)kMaxDynSmem - 1024 - kCtlBytes;
   pl->num_k_blocks = (int)(pl->k / kTileK);
-  if (best_bh > 0 && force_path != kPathRows) {
+  if (best_bh > 0 && c.path != 1) {
     pl->key.path = kPathSwap;
     pl->key.bn = kTileM;
     pl->key.cm = 1;
@@ -213,27 +346,33 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     // per SM: k blocks x (Y box + X rows) + 4.4 x the partial's bytes (a
     // partial is written and read back at about half the load rate).
     const int max_splits = std::min(16, pl->num_k_blocks);
-    const int env_groups = env_int("AGMM_ROWGROUPS", 0);
-    const int env_splits = env_int("AGMM_SPLITK", 0);
-    int best_g = 1, best_s = 1;
-    double best_model = -1.0;
-    for (int G = 1; G <= pl->total_chunks; G *= 2) {
-      if (env_groups > 0 && G != env_groups) continue;
-      const int cpg = (pl->total_chunks + G - 1) / G;
-      if ((G - 1) * cpg >= pl->total_chunks) continue;  // the last group would be empty
-      const int gcols = cpg * pl->box_rows;
-      int S = pl->num_sms / (pl->num_n_tiles * G);
-      S = std::max(1, std::min(S, max_splits));
-      if (env_splits > 0) S = std::max(1, std::min(env_splits, max_splits));
-      const int kb = (pl->num_k_blocks + S - 1) / S;
-      const int mn = (gcols + 31) / 32 * 32;
-      const double model = (double)kb * (kASlotBytes + 128.0 * mn) + (S > 1 ? 4.4 * 512.0 * gcols : 0.0);
-      if (best_model < 0 || model < best_model * 0.97) {
-        best_model = model;
-        best_g = G;
-        best_s = S;
+    auto pick_groups = [&](int force_g, int* out_g, int* out_s) {
+      double best_model = -1.0;
+      for (int G = 1; G <= pl->total_chunks; G *= 2) {
+        if (force_g > 0 && G != force_g) continue;
+        const int cpg = (pl->total_chunks + G - 1) / G;
+        if ((G - 1) * cpg >= pl->total_chunks) continue;  // the last group would be empty
+        const int gcols = cpg * pl->box_rows;
+        int S = pl->num_sms / (pl->num_n_tiles * G);
+        S = std::max(1, std::min(S, max_splits));
+        if (c.splits > 0) S = std::max(1, std::min(c.splits, max_splits));
+        const int kb = (pl->num_k_blocks + S - 1) / S;
+        const int mn = (gcols + 31) / 32 * 32;
+        const double model = (double)kb * (kASlotBytes + 128.0 * mn) + (S > 1 ? 4.4 * 512.0 * gcols : 0.0);
+        if (best_model < 0 || model < best_model * 0.97) {
+          best_model = model;
+          *out_g = G;
+          *out_s = S;
+        }
+        if (force_g == 0 && G >= 8) break;
       }
-      if (env_groups == 0 && G >= 8) break;
+      return best_model >= 0;
+    };
+    int best_g = 1, best_s = 1;
+    if (!pick_groups(c.row_groups, &best_g, &best_s)) {
+      if (strict.row_groups != 0)
+        return fail(AGMM_ERR_UNSUPPORTED, "config.row_groups leaves a row group empty for this shape");
+      pick_groups(0, &best_g, &best_s);
     }
     pl->row_groups = best_g;
     pl->group_chunks = (pl->total_chunks + best_g - 1) / best_g;
@@ -241,13 +380,13 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->b_slot_bytes = (uint32_t)pl->mma_n * 128u;
     const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
     pl->stages = (int)std::min<int64_t>(kMaxStages, budget / stage_bytes);
-    pl->stages = std::min(pl->stages, std::max(2, env_int("AGMM_STAGES", kMaxStages)));
+    if (c.stages) pl->stages = std::min(pl->stages, c.stages);
     // The k splits (cluster size); plan_impl lowers them until one wave of
     // clusters covers every (n tile, row group).
     pl->splits = best_s;
-    // k-split partials go through device memory (L2) unless AGMM_SWAP_DSMEM=1
+    // k-split partials go through device memory (L2) unless dsmem_reduce
     // routes them through distributed shared memory.
-    pl->swap_dsmem = env_int("AGMM_SWAP_DSMEM", 0) != 0;
+    pl->swap_dsmem = c.dsmem_reduce == AGMM_CFG_ON;
     pl->tmem_cols = pow2_ceil(std::max(32, pl->mma_n));
     pl->group_m = 1;
   } else {
@@ -257,7 +396,7 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     // box (fewest TMA boxes per stage); ties keep the half split.
     int64_t min_tiles = -1;
     for (int whole = whole_lo; whole <= whole_hi; ++whole)
-      for (int bh = 128; bh >= 8; bh >>= 1) {
+      for (int bh = bh_top; bh >= bh_bottom; bh >>= 1) {
         const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh, whole);
         const int64_t t = (ring_total_chunks(g) + kTileM / bh - 1) / (kTileM / bh);
         if (min_tiles < 0 || t < min_tiles) min_tiles = t;
@@ -265,7 +404,7 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     int bh_best = -1, whole_best = 0;
     int64_t tiles_best = -1;
     for (int whole = whole_lo; whole <= whole_hi; ++whole)
-      for (int bh = 128; bh >= 8; bh >>= 1) {
+      for (int bh = bh_top; bh >= bh_bottom; bh >>= 1) {
         const RingGeom g = make_ring_geom(pl->P, pl->m_pd, 0, bh, whole);
         const int64_t t = (ring_total_chunks(g) + kTileM / bh - 1) / (kTileM / bh);
         if (t * 100 > min_tiles * 103 && t > min_tiles) continue;
@@ -277,8 +416,12 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
       }
     if (tiles_best > (int64_t)1 << 30) return fail(AGMM_ERR_INVALID_ARG, "too many row tiles");
     int bn = (pl->n % 256 == 0) ? 256 : 128;
-    const int env_bn = env_int("AGMM_BN", 0);
-    if ((env_bn == 128 || env_bn == 256) && pl->n % env_bn == 0) bn = env_bn;
+    if (c.tile_n) {
+      if (pl->n % c.tile_n == 0)
+        bn = c.tile_n;
+      else if (strict.tile_n)
+        return fail(AGMM_ERR_UNSUPPORTED, "config.tile_n does not divide n");
+    }
     pl->key.bn = bn;
     pl->box_rows = bh_best;
     pl->whole_shards = whole_best;
@@ -287,16 +430,16 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->num_n_tiles = (int)(pl->n / bn);
     // Clusters of two CTAs on neighbouring row tiles share each Y tile through
     // TMA multicast (each loads half), cutting per-SM operand traffic by a third.
-    int cm = pl->num_m_tiles >= 2 ? 2 : 1;
-    const int env_cm = env_int("AGMM_CM", 0);
-    if (env_cm == 1 || env_cm == 2) cm = env_cm;
+    const int cm = c.cluster_m ? c.cluster_m : (pl->num_m_tiles >= 2 ? 2 : 1);
     pl->key.cm = cm;
     // Two-CTA clusters either multiply alone with the Y tile multicast (the
-    // default) or, with AGMM_PAIR=1, as a cta_group::2 pair in which each CTA
+    // default) or, with cta_pair on, as a cta_group::2 pair in which each CTA
     // holds its 128 rows and half the Y tile (32 KiB per k block and SM instead
     // of 48 KiB).  On GB300 the pair measured no faster for Y stored [n, k] and
     // slower for Y stored [k, n], so it stays opt-in.
-    pl->key.pair = cm == 2 && env_int("AGMM_PAIR", 0) != 0;
+    if (c.cta_pair == AGMM_CFG_ON && cm != 2 && strict.cta_pair == AGMM_CFG_ON)
+      return fail(AGMM_ERR_UNSUPPORTED, "config.cta_pair needs cluster_m 2");
+    pl->key.pair = cm == 2 && c.cta_pair == AGMM_CFG_ON;
     pl->num_mc_tiles = (pl->num_m_tiles + cm - 1) / cm;
     if ((int64_t)pl->num_mc_tiles * pl->num_n_tiles > ((int64_t)1 << 31) - 1)
       return fail(AGMM_ERR_INVALID_ARG, "too many output tiles");
@@ -305,20 +448,53 @@ agmm_status_t choose_tiles(agmm_plan_s* pl) {
     pl->b_slot_bytes = (uint32_t)(pl->key.pair ? bn / 2 : bn) * 128u;
     const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
     pl->stages = (int)std::min<int64_t>(kMaxStages, budget / stage_bytes);
-    pl->stages = std::min(pl->stages, std::max(2, env_int("AGMM_STAGES", kMaxStages)));
+    if (c.stages) pl->stages = std::min(pl->stages, c.stages);
     pl->splits = 1;
     pl->tmem_cols = 2 * bn;
-    pl->group_m = std::max(1, env_int("AGMM_GROUP_M", 8));
+    pl->group_m = c.group_m ? c.group_m : 8;
+    pl->stream_k = c.stream_k != AGMM_CFG_OFF;
   }
   pl->smem_bytes = tmem_safe_smem(1024 + (size_t)pl->stages * (kASlotBytes + pl->b_slot_bytes) + kCtlBytes,
                                   pl->tmem_cols);
   return AGMM_OK;
 }
 
+// Rows path: persistent clusters, one CTA per SM, at most `max_clusters`
+// co-resident.  Whole waves of cluster tiles are dealt round-robin; when the
+// tile count is not a multiple of the clusters, the last one to two waves' k
+// blocks are divided evenly over the clusters (stream-K), so no SM idles in a
+// ragged last wave.
+void size_rows_grid(agmm_plan_s* pl, int max_clusters) {
+  const int cm = pl->key.cm;
+  int G = std::max(1, std::min(pl->num_sms / cm, max_clusters));
+  const int T = pl->num_tiles;
+  int dp = T;
+  if (T % G != 0 && pl->stream_k) {
+    // Stream-K over the ragged last wave alone keeps its tiles together in
+    // raster order (L2 reuse) as long as a tile is shared by at most about
+    // three clusters; a thinner last wave also takes the wave before it.
+    const int W = T / G;
+    const int R = T - W * G;
+    dp = (W >= 1 && 3 * R >= G) ? W * G : (W >= 1 ? (W - 1) * G : 0);
+    // at least 4 k blocks per cluster share
+    const int64_t units = (int64_t)(T - dp) * pl->num_k_blocks;
+    if (units < (int64_t)G * 4) G = (int)std::max<int64_t>(1, units / 4);
+  }
+  if (dp == T) G = std::min(G, T);
+  pl->dp_tiles = dp;
+  pl->sk_tiles = T - dp;
+  pl->grid = dim3((unsigned)(G * cm), 1, 1);
+  pl->tail_bytes = pl->sk_tiles > 0 ? (size_t)(pl->sk_tiles * cm * 4 + 255) / 256 * 256 +
+                                          (size_t)G * cm * kTileM * (size_t)pl->key.bn * 4
+                                    : 0;
+  pl->cluster_x = cm;
+}
+
 agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t dtype, int rhs_t,
-                        bool with_sub, agmm_plan_s** out) {
+                        const agmm_tile_config_t* config, bool with_sub, agmm_plan_s** out) {
   agmm_status_t st = validate_shape(P, m_pd, k, n, (int)dtype, rhs_t);
   if (st != AGMM_OK) return st;
+  if ((st = validate_config(config)) != AGMM_OK) return st;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
@@ -350,7 +526,9 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   pl->key.out_f32 = dtype == AGMM_BF16_F32OUT || dtype == AGMM_F16_F32OUT;
   pl->f16 = dtype == AGMM_F16 || dtype == AGMM_F16_F32OUT;
   pl->out_elem = pl->key.out_f32 ? 4 : 2;
-  st = choose_tiles(pl);
+  const ResolvedConfig rc = resolve_config(pl, config);
+  pl->config_source = rc.source;
+  st = choose_tiles(pl, rc.cfg, rc.strict);
   if (st != AGMM_OK) {
     delete pl;
     return st;
@@ -414,33 +592,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       pl->tail_bytes = (size_t)pl->num_n_tiles * pl->row_groups * pl->splits * groups * 4 * kTileM * 16;
     }
   } else {
-    // Persistent clusters, one CTA per SM.  Whole waves of cluster tiles are
-    // dealt round-robin; when the tile count is not a multiple of the
-    // clusters, the last one to two waves' k blocks are divided evenly over
-    // the clusters (stream-K), so no SM idles in a ragged last wave.
-    const int cm = pl->key.cm;
-    int G = std::max(1, std::min(pl->num_sms / cm, pl->max_clusters));
-    const int T = pl->num_tiles;
-    int dp = T;
-    if (T % G != 0 && env_int("AGMM_STREAMK", 1) != 0) {
-      // Stream-K over the ragged last wave alone keeps its tiles together in
-      // raster order (L2 reuse) as long as a tile is shared by at most about
-      // three clusters; a thinner last wave also takes the wave before it.
-      const int W = T / G;
-      const int R = T - W * G;
-      dp = (W >= 1 && 3 * R >= G) ? W * G : (W >= 1 ? (W - 1) * G : 0);
-      // at least 4 k blocks per cluster share
-      const int64_t units = (int64_t)(T - dp) * pl->num_k_blocks;
-      if (units < (int64_t)G * 4) G = (int)std::max<int64_t>(1, units / 4);
-    }
-    if (dp == T) G = std::min(G, T);
-    pl->dp_tiles = dp;
-    pl->sk_tiles = T - dp;
-    pl->grid = dim3((unsigned)(G * cm), 1, 1);
-    pl->tail_bytes = pl->sk_tiles > 0 ? (size_t)(pl->sk_tiles * cm * 4 + 255) / 256 * 256 +
-                                            (size_t)G * cm * kTileM * (size_t)pl->key.bn * 4
-                                      : 0;
-    pl->cluster_x = cm;
+    size_rows_grid(pl, pl->max_clusters);
   }
   KernelParams& kp = pl->params;
   kp.m_pd = m_pd;
@@ -471,7 +623,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.f16 = pl->f16 ? 1 : 0;
   kp.dp_tiles = pl->dp_tiles;
   if (with_sub && P > 1) {
-    st = plan_impl(1, pl->M(), k, n, dtype, rhs_t, false, &pl->sub);
+    st = plan_impl(1, pl->M(), k, n, dtype, rhs_t, nullptr, false, &pl->sub);
     if (st != AGMM_OK) {
       delete pl;
       return st;
@@ -615,14 +767,19 @@ agmm_status_t run_unfused_on_scratch(agmm_plan_s* plan, const void* const* x_sha
 
 extern "C" {
 
-agmm_status_t agmm_plan(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
-                        int rhs_transpose, agmm_plan_t* out_plan) {
+agmm_status_t agmm_plan_config(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
+                               int rhs_transpose, const agmm_tile_config_t* config, agmm_plan_t* out_plan) {
   if (!out_plan) return fail(AGMM_ERR_INVALID_ARG, "out_plan is NULL");
   *out_plan = nullptr;
   agmm_plan_s* pl = nullptr;
-  agmm_status_t st = plan_impl(P, m_per_device, k, n, dtype, rhs_transpose, true, &pl);
+  agmm_status_t st = plan_impl(P, m_per_device, k, n, dtype, rhs_transpose, config, true, &pl);
   if (st == AGMM_OK) *out_plan = pl;
   return st;
+}
+
+agmm_status_t agmm_plan(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
+                        int rhs_transpose, agmm_plan_t* out_plan) {
+  return agmm_plan_config(P, m_per_device, k, n, dtype, rhs_transpose, nullptr, out_plan);
 }
 
 void agmm_destroy(agmm_plan_t plan) {
@@ -768,15 +925,22 @@ agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info) {
   info->num_sms = plan->num_sms;
   info->smem_bytes = plan->smem_bytes;
   info->row_groups = plan->key.path == kPathSwap ? plan->row_groups : 1;
+  info->cluster_m = plan->key.path == kPathSwap ? 1 : plan->key.cm;
+  info->cta_pair = plan->key.pair ? 1 : 0;
+  info->stream_k_tiles = plan->key.path == kPathSwap ? 0 : plan->sk_tiles;
+  info->dsmem_reduce = plan->key.path == kPathSwap && plan->swap_dsmem ? 1 : 0;
+  info->config_source = plan->config_source;
   return AGMM_OK;
 }
 
 agmm_status_t agmm_plan_preview(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
-                                int rhs_transpose, int num_sms, agmm_plan_info_t* info) {
+                                int rhs_transpose, const agmm_tile_config_t* config, int num_sms,
+                                agmm_plan_info_t* info) {
   if (!info) return fail(AGMM_ERR_INVALID_ARG, "info is NULL");
   if (num_sms < 1 || num_sms > 4096) return fail(AGMM_ERR_INVALID_ARG, "num_sms must be in [1, 4096]");
   agmm_status_t st = validate_shape(P, m_per_device, k, n, (int)dtype, rhs_transpose);
   if (st != AGMM_OK) return st;
+  if ((st = validate_config(config)) != AGMM_OK) return st;
   agmm_plan_s pl;
   pl.P = P;
   pl.m_pd = m_per_device;
@@ -788,8 +952,11 @@ agmm_status_t agmm_plan_preview(int P, int64_t m_per_device, int64_t k, int64_t 
   pl.key.y_kmajor = rhs_transpose != 0;
   pl.key.out_f32 = dtype == AGMM_BF16_F32OUT || dtype == AGMM_F16_F32OUT;
   pl.f16 = dtype == AGMM_F16 || dtype == AGMM_F16_F32OUT;
-  st = choose_tiles(&pl);
+  const ResolvedConfig rc = resolve_config(&pl, config);
+  st = choose_tiles(&pl, rc.cfg, rc.strict);
   if (st != AGMM_OK) return st;
+  // the row path's grid as if every cluster were resident
+  if (pl.key.path == kPathRows) size_rows_grid(&pl, num_sms / pl.key.cm);
   info->path = pl.key.path;
   info->box_rows = pl.box_rows;
   info->whole_shards = pl.whole_shards;
@@ -800,13 +967,17 @@ agmm_status_t agmm_plan_preview(int P, int64_t m_per_device, int64_t k, int64_t 
   info->stages = pl.stages;
   info->splits = pl.splits;
   info->num_tiles = pl.num_tiles;
-  const int cm = pl.key.path == kPathSwap ? 1 : pl.key.cm;
   info->num_ctas = pl.key.path == kPathSwap ? pl.splits * pl.num_n_tiles * pl.row_groups
-                                            : std::min(pl.num_tiles * cm, (num_sms / cm) * cm);
+                                            : (int)(pl.grid.x * pl.grid.y * pl.grid.z);
   info->group_m = pl.group_m;
   info->num_sms = num_sms;
   info->smem_bytes = pl.smem_bytes;
   info->row_groups = pl.key.path == kPathSwap ? pl.row_groups : 1;
+  info->cluster_m = pl.key.path == kPathSwap ? 1 : pl.key.cm;
+  info->cta_pair = pl.key.pair ? 1 : 0;
+  info->stream_k_tiles = pl.key.path == kPathSwap ? 0 : pl.sk_tiles;
+  info->dsmem_reduce = pl.key.path == kPathSwap && pl.swap_dsmem ? 1 : 0;
+  info->config_source = rc.source;
   return AGMM_OK;
 }
 

@@ -85,7 +85,53 @@ typedef struct {
   int num_sms;       /* SMs of the planned device                                */
   size_t smem_bytes; /* dynamic shared memory per CTA                            */
   int row_groups;    /* swapped tiles: groups of chunks, one MMA N each (else 1) */
+  int cluster_m;     /* row tiles: CTAs per cluster sharing a Y tile (else 1)    */
+  int cta_pair;      /* row tiles: 1 when a cluster multiplies as a CTA pair     */
+  int stream_k_tiles;/* row tiles: output tiles whose k blocks are shared        */
+  int dsmem_reduce;  /* swapped tiles: 1 when k-split partials go through
+                        distributed shared memory, 0 through device memory     */
+  int config_source; /* 0: the planner's rules; 1: the tuned table (an entry
+                        measured for this exact shape); 2: a caller's config or
+                        AGMM_* environment overrides set at least one field     */
 } agmm_plan_info_t;
+
+/*
+ * Tile configuration for agmm_plan_config and agmm_plan_preview.
+ * all_gather_matmul (tpu_inference "all_gather_matmul.py") takes its block
+ * sizes bn and bk as optional arguments and fills the missing ones from a
+ * table of tuned sizes keyed by shape, dtype and mesh size
+ * (get_tuned_block_sizes); this struct is that argument.  Every field left at
+ * 0 (AGMM_CFG_AUTO) is chosen by the planner: from the tuned table when it
+ * holds an entry for the exact (P, m_per_device, k, n, rhs_transpose, input
+ * type), else by its rules.  On/off fields take AGMM_CFG_OFF or
+ * AGMM_CFG_ON.  Fields that belong to the other tile path are ignored.
+ */
+#define AGMM_CFG_AUTO 0
+#define AGMM_CFG_OFF 1
+#define AGMM_CFG_ON 2
+typedef struct {
+  int path;         /* 1: row tiles; 2: swapped tiles (needs every gathered row,
+                       padded to box heights, within 256)                     */
+  int chunks;       /* 1: the ring's half-shard chunks; 2: whole-shard chunks */
+  int box_rows;     /* X rows per TMA box: 8, 16, 32, 64 or 128               */
+  int tile_n;       /* row tiles: MMA N, 128 or 256 (n must be a multiple)    */
+  int cluster_m;    /* row tiles: 1, or 2 neighbouring row tiles per cluster
+                       sharing each Y tile by TMA multicast                   */
+  int cta_pair;     /* row tiles: on = a 2-CTA cluster multiplies as one
+                       cta_group::2 pair (needs cluster_m 2)                  */
+  int stages;       /* pipeline stages, 2..8: an upper bound that shared
+                       memory may lower (a swapped k-split reduction that
+                       receives in shared memory may raise it)                */
+  int group_m;      /* row tiles: row-tile (pairs) per raster group, >= 1     */
+  int stream_k;     /* row tiles: share a ragged last wave's k blocks         */
+  int row_groups;   /* swapped tiles: groups of chunks (1, 2, 4, ...), each a
+                       separate MMA N; no group may be empty                  */
+  int splits;       /* swapped tiles: k splits per cluster, 1..16: an upper
+                       bound, lowered until every cluster is resident         */
+  int dsmem_reduce; /* swapped tiles: on = reduce the k splits through
+                       distributed shared memory instead of device memory     */
+  int tuned_table;  /* off = ignore the tuned table for this plan             */
+} agmm_tile_config_t;
 
 /*
  * agmm_plan -- validate a problem and choose tiles for the current device.
@@ -107,6 +153,19 @@ typedef struct {
  */
 agmm_status_t agmm_plan(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
                         int rhs_transpose, agmm_plan_t* out_plan);
+
+/*
+ * agmm_plan_config -- agmm_plan with a tile configuration.  Fields of
+ * `config` that are set take precedence over the AGMM_* environment
+ * overrides, which take precedence over the tuned table.  NULL behaves like
+ * agmm_plan.  Returns AGMM_ERR_INVALID_ARG for a field outside its range, and
+ * AGMM_ERR_UNSUPPORTED when a set field cannot hold for this shape (swapped
+ * tiles for more than 256 padded rows, tile_n not dividing n, a CTA pair
+ * without a 2-CTA cluster, an empty row group, a box height whose swapped
+ * rows exceed 256).
+ */
+agmm_status_t agmm_plan_config(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
+                               int rhs_transpose, const agmm_tile_config_t* config, agmm_plan_t* out_plan);
 
 /* Release a plan.  NULL is a no-op. */
 void agmm_destroy(agmm_plan_t plan);
@@ -240,11 +299,13 @@ agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info);
  * agmm_plan.  The device-dependent steps that agmm_plan adds afterwards are
  * absent: lowering the k splits until every cluster is resident, and
  * sizing the row path's persistent grid.  So `splits` is an upper bound and
- * `num_ctas` is the grid before them.  Returns AGMM_ERR_INVALID_ARG for a
+ * `num_ctas` is the grid before them.  `config` (NULL allowed) acts as in
+ * agmm_plan_config, with the same errors.  Returns AGMM_ERR_INVALID_ARG for a
  * NULL info or num_sms outside [1, 4096].
  */
 agmm_status_t agmm_plan_preview(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,
-                                int rhs_transpose, int num_sms, agmm_plan_info_t* info);
+                                int rhs_transpose, const agmm_tile_config_t* config, int num_sms,
+                                agmm_plan_info_t* info);
 
 /*
  * The ring-ordered row sequence, host side (no device needed).  For box

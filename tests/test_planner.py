@@ -21,7 +21,9 @@ def _library(agmm_lib):
 
 
 def preview(w, **kw):
-    return agmm.plan_preview(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, num_sms=SMS, **kw)
+    # the planner's own rules: the tuned table is switched off
+    return agmm.plan_preview(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, num_sms=SMS,
+                             config={"tuned_table": False}, **kw)
 
 
 # (path, box_rows, whole_shards, chunks, tile_n, stages, row_groups, split bound)
@@ -110,11 +112,11 @@ def test_environment_overrides(monkeypatch):
 def test_preview_argument_errors():
     lib = agmm.load_library()
     info = agmm.PlanInfo()
-    assert lib.agmm_plan_preview(2, 16, 256, 128, 0, 0, 0, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
-    assert lib.agmm_plan_preview(2, 16, 256, 128, 0, 0, 152, None) == agmm.AGMM_ERR_INVALID_ARG
-    assert lib.agmm_plan_preview(2, 16, 200, 128, 0, 0, 152, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
-    assert lib.agmm_plan_preview(9, 16, 256, 128, 0, 0, 152, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
-    assert lib.agmm_plan_preview(2, 16, 256, 128, 5, 0, 152, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
+    assert lib.agmm_plan_preview(2, 16, 256, 128, 0, 0, None, 0, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
+    assert lib.agmm_plan_preview(2, 16, 256, 128, 0, 0, None, 152, None) == agmm.AGMM_ERR_INVALID_ARG
+    assert lib.agmm_plan_preview(2, 16, 200, 128, 0, 0, None, 152, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
+    assert lib.agmm_plan_preview(9, 16, 256, 128, 0, 0, None, 152, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
+    assert lib.agmm_plan_preview(2, 16, 256, 128, 5, 0, None, 152, ctypes.byref(info)) == agmm.AGMM_ERR_INVALID_ARG
 
 
 def _tmem_cols(info):
