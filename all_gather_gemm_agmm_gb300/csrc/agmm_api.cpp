@@ -96,6 +96,30 @@ bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer
   return true;
 }
 
+// Y stored [k, n] as a 3-D tensor: dims {64 n, k, n / 64}, byte strides
+// {n * 2, 128}; a box {64, 64, blocks} brings `blocks` 64-column blocks of
+// one 64-row k block, each an 8 KiB MN-major swizzled block, in one copy.
+bool encode_y_mn3d(CUtensorMap* map, const void* ptr, uint64_t n, uint64_t k, uint32_t blocks, bool f16,
+                   std::string* err) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  cuuint64_t dims[3] = {64, k, n / 64};
+  cuuint64_t strides[2] = {n * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTileK, blocks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled (3-D Y) failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
 }  // namespace
 
 struct agmm_plan_s {
@@ -685,10 +709,23 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
     bool ok;
     const uint32_t y_rows =
         pl->key.path == kPathSwap ? (uint32_t)kTileM : (uint32_t)(pl->key.bn / pl->key.cm);
-    if (pl->rhs_t)  // Y [n, k]: K-major boxes of y_rows n-rows
+    kp.y3d = 0;
+    if (pl->rhs_t) {  // Y [n, k]: K-major boxes of y_rows n-rows
       ok = encode_2d(&kp.ymap, y, (uint64_t)pl->k, (uint64_t)pl->n, kTileK, y_rows, pl->f16, &err);
-    else  // Y [k, n]: MN-major boxes of 64 n x 64 k
-      ok = encode_2d(&kp.ymap, y, (uint64_t)pl->n, (uint64_t)pl->k, 64, kTileK, pl->f16, &err);
+    } else {
+      // Y [k, n]: MN-major 64 n x 64 k blocks, all of one load (y_rows
+      // columns) in one 3-D box; one 2-D box per block if the driver
+      // refuses the 3-D map.
+      ok = env_int("AGMM_Y3D", 1) != 0 &&
+           encode_y_mn3d(&kp.ymap, y, (uint64_t)pl->n, (uint64_t)pl->k, y_rows / 64, pl->f16, &err);
+      if (ok) {
+        kp.y3d = 1;
+      } else {
+        if (!err.empty() && std::getenv("AGMM_LOG")) std::fprintf(stderr, "[agmm] %s; using 2-D boxes\n", err.c_str());
+        err.clear();
+        ok = encode_2d(&kp.ymap, y, (uint64_t)pl->n, (uint64_t)pl->k, 64, kTileK, pl->f16, &err);
+      }
+    }
     if (!ok) {
       pl->cache_valid = false;
       return fail(AGMM_ERR_CUDA, "Y tensor map: " + err);

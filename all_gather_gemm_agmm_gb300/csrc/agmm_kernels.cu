@@ -523,6 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
               if constexpr (kCM == 1) {
                 if constexpr (kYK) {
                   ptx::tma_load_2d(b_dst, &p.ymap, full, k0, nt * kBN);
+                } else if (p.y3d) {
+                  ptx::tma_load_3d(b_dst, &p.ymap, full, 0, k0, nt * (kBN / 64));
                 } else {
 #pragma unroll
                   for (int a = 0; a < kBN / 64; ++a)
@@ -535,6 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
                     ptx::tma_load_2d_pair(b_dst, &p.ymap, full, k0, nt * kBN + crank * (kBN / 2));
                   else
                     ptx::tma_load_2d(b_dst, &p.ymap, full, k0, nt * kBN + crank * (kBN / 2));
+                } else if (p.y3d) {
+                  constexpr int kBoxes = kBN / 64 / 2;
+                  if (to_leader)
+                    ptx::tma_load_3d_pair(b_dst, &p.ymap, full, 0, k0, nt * (kBN / 64) + crank * kBoxes);
+                  else
+                    ptx::tma_load_3d(b_dst, &p.ymap, full, 0, k0, nt * (kBN / 64) + crank * kBoxes);
                 } else {
                   constexpr int kBoxes = kBN / 64 / 2;
 #pragma unroll
@@ -553,6 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
                   constexpr int kRows = kBN / kCM;
                   ptx::tma_load_2d_multicast(b_dst + (uint32_t)(crank * kRows) * 128u, &p.ymap, full, k0,
                                              nt * kBN + crank * kRows, cmask);
+                } else if (p.y3d) {
+                  constexpr int kBoxes = kBN / 64 / kCM;
+                  ptx::tma_load_3d_multicast(b_dst + (uint32_t)(crank * kBoxes) * 8192u, &p.ymap, full, 0, k0,
+                                             nt * (kBN / 64) + crank * kBoxes, cmask);
                 } else {
                   constexpr int kBoxes = kBN / 64 / kCM;
 #pragma unroll
@@ -566,6 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             } else {
               if constexpr (kYK) {
                 ptx::tma_load_2d(a_dst, &p.ymap, full, k0, nt * kTileM);
+              } else if (p.y3d) {
+                ptx::tma_load_3d(a_dst, &p.ymap, full, 0, k0, nt * (kTileM / 64));
               } else {
 #pragma unroll
                 for (int a = 0; a < kTileM / 64; ++a)

@@ -28,7 +28,8 @@ enum StatusRole : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRol
 
 struct __align__(128) KernelParams {
   CUtensorMap xmap[kMaxShards];  // shard r: [m_pd, k] bf16, box {64, box_rows}, 128B swizzle
-  CUtensorMap ymap;              // Y: K-major box {64, rows} or MN-major box {64, 64}
+  CUtensorMap ymap;              // Y: K-major box {64, rows}; MN-major box {64, 64} or,
+                                 // with y3d, {64, 64, blocks} over dims {64, k, n / 64}
   void* out;                     // O [P*m_pd, n], bf16 or f32
   int* status;                   // status words (may be null)
   int64_t m_pd;                  // rows per shard
@@ -78,6 +79,7 @@ struct __align__(128) KernelParams {
   // tile whose share of the k range holds it.
   CUtensorMap xcatmap[kMaxShards];
   int store_xcat;
+  int y3d;                       // Y [k, n]: one 3-D box per load instead of one 2-D box per 64 columns
 };
 
 struct GatherParams {

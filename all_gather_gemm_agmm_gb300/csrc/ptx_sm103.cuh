@@ -131,6 +131,37 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* 
       : "memory");
 }
 
+// 3-D tiled loads (c0 innermost).  For Y stored [k, n], a map with dims
+// {64 n, k, n / 64} (strides n * 2 and 128 bytes) delivers several 64-column
+// blocks of one k block in one box, laid out as consecutive 8 KiB blocks:
+// the shared-memory image of as many 2-D boxes, for one copy instruction.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const void* map, uint32_t bar, int c0,
+                                                      int c1, int c2, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* map, uint32_t bar, int c0, int c1,
+                                                 int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
 // Tensor copy into this CTA's shared memory whose completion is counted on an
 // mbarrier of the CTA pair (cta_group::2): `bar` is a shared::cluster address,
 // here the pair leader's barrier.
