@@ -78,22 +78,34 @@ __device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
     return ptx::mbar_try_wait(bar, parity);
 }
 
+// Suspend-time hint of the waits' retries: a waiting thread sleeps until the
+// phase completes or this long passes (the abort flag and the bound are
+// checked between sleeps).
+constexpr uint32_t kSleepHintNs = 20000;
+
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool try_wait_sleep(uint32_t bar, uint32_t parity) {
+  if constexpr (kClusterScope)
+    return ptx::mbar_try_wait_cluster_sleep(bar, parity, kSleepHintNs);
+  else
+    return ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs);
+}
+
 // The bound is in SM clock cycles (the host converts the time limit at the
-// device's peak clock, so a wait lasts at least that long).
+// device's peak clock, so a wait lasts at least that long).  The first test
+// returns at once; the retries sleep on the barrier rather than poll it.
 template <bool kClusterScope = false>
 __device__ __forceinline__ int wait_phase(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_cycles, uint64_t* waited = nullptr) {
   if (try_wait_scoped<kClusterScope>(bar, parity)) return kWaitOk;
   const uint64_t t0 = ptx::clock_cycles();
-  for (uint32_t it = 1;; ++it) {
-    if (try_wait_scoped<kClusterScope>(bar, parity)) {
+  for (;;) {
+    if (try_wait_sleep<kClusterScope>(bar, parity)) {
       if (waited) *waited += ptx::clock_cycles() - t0;
       return kWaitOk;
     }
-    if ((it & 15u) == 0u) {
-      if (*abort) return kWaitAborted;
-      if (ptx::clock_cycles() - t0 > limit_cycles) return kWaitTimeout;
-    }
+    if (*abort) return kWaitAborted;
+    if (ptx::clock_cycles() - t0 > limit_cycles) return kWaitTimeout;
   }
 }
 
@@ -106,9 +118,9 @@ __device__ __forceinline__ void trace_value(const KernelParams& p, int slot, uin
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_cycles) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::clock_cycles();
-  for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0u && ptx::clock_cycles() - t0 > limit_cycles) return false;
+  for (;;) {
+    if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (ptx::clock_cycles() - t0 > limit_cycles) return false;
   }
 }
 
