@@ -457,7 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues the copies and
+    // the barrier arrivals.
+    {
+      const bool leader = ptx::elect_one();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;
@@ -501,25 +504,29 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           bytes = (uint32_t)kASlotBytes + (uint32_t)swap_nch * p.box_rows * 128u;
         }
         for (int kb = kb0; kb < kb1; ++kb) {
-          const int res = wait_phase(bar_empty(ctl, stage), phase ^ 1u, abort_flag, limit, wait_acc);
+          int res = wait_phase(bar_empty(ctl, stage), phase ^ 1u, abort_flag, limit, wait_acc);
+          res = __shfl_sync(0xffffffffu, res, 0);
           if (res != kWaitOk) {
-            record_failure(p, abort_flag, res, kRoleProducer, stage, tile);
+            if (leader) record_failure(p, abort_flag, res, kRoleProducer, stage, tile);
             ok = false;
             break;
           }
           // A pair follower's copies complete on the leader's barrier.
           const bool to_leader = kPair && crank == 1;
           const uint32_t full = to_leader ? ptx::map_shared_rank(bar_full(ctl, stage), 0) : bar_full(ctl, stage);
-          if (p.test_drop_first_arrive && !dropped) {
-            dropped = true;  // the MMA thread's wait on this stage runs out
-          } else {
-            if (to_leader) {
+          // test hook: the first arrival is dropped, so the MMA thread's wait
+          // on this stage runs out
+          const bool drop = p.test_drop_first_arrive && !dropped;
+          if (drop) dropped = true;
+          if (!drop && !to_leader) {
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (!drop && leader) {
+            if (to_leader)
               ptx::mbar_arrive_expect_tx_remote(full, bytes);
-            } else {
+            else
               ptx::mbar_arrive_expect_tx(full, bytes);
-              armed |= 1u << stage;
-              armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-            }
             const uint32_t a_dst = a0 + (uint32_t)stage * kASlotBytes;
             const uint32_t b_dst = b0 + (uint32_t)stage * p.b_slot_bytes;
             const int k0 = kb * kTileK;
@@ -615,20 +622,26 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         }
       }
       trace(p, 3);
-      if (kPath == kPathRows) trace_value(p, 10, waited_empty);
-      // Wait for this thread's TMA loads still in flight (only on an abort can
-      // a load be unconsumed; a consumed stage's phase has already completed).
-      for (int s = 0; s < S; ++s)
-        if ((armed >> s) & 1u)
-          if (!wait_drain(bar_full(ctl, s), (armed_parity >> s) & 1u, limit))
-            record_failure(p, abort_flag, kWaitTimeout, kRoleDrain, s, -1);
+      if (leader) {
+        if (kPath == kPathRows) trace_value(p, 10, waited_empty);
+        // Wait for the TMA loads still in flight (only on an abort can a load
+        // be unconsumed; a consumed stage's phase has already completed).
+        for (int s = 0; s < S; ++s)
+          if ((armed >> s) & 1u)
+            if (!wait_drain(bar_full(ctl, s), (armed_parity >> s) & 1u, limit))
+              record_failure(p, abort_flag, kWaitTimeout, kRoleDrain, s, -1);
+      }
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (kPair && crank == 1) {
       // Pair follower: the leader's MMA thread works for both CTAs; the
       // follower's copies complete on the leader's stage barriers.
-    } else if (lane == 0) {
+    } else {
+      // The whole warp runs the loop; one elected lane issues the MMAs,
+      // commits and bulk copies.
+      const bool issuer = ptx::elect_one();
       constexpr int kN = (kPath == kPathRows) ? kBN : 0;
       const int mma_n = (kPath == kPathRows) ? kN : p.mma_n;
       // rows path: A = X chunks (K-major), B = Y; swap path: A = Y, B = X chunks.
@@ -676,25 +689,35 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         int res = wait_phase<kCS>(bar_acc_empty(ctl, acc), acc_phase ^ 1u, abort_flag, limit, wa);
+        res = __shfl_sync(0xffffffffu, res, 0);
         if (res != kWaitOk) {
-          record_failure(p, abort_flag, res, kRoleMma, -1, tile);
+          if (issuer) record_failure(p, abort_flag, res, kRoleMma, -1, tile);
           break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * mma_n);
+        // The next stage's full barrier is tested while this stage's MMAs
+        // are issued, so its latency is off the loop's critical path.
+        bool full_ready = false;
         for (int kb = kb0; kb < kb1; ++kb) {
           // (a pair: this barrier also counts the follower's copies)
-          res = wait_phase(bar_full(ctl, stage), phase, abort_flag, limit, wf);
-          if (res != kWaitOk) {
-            record_failure(p, abort_flag, res, kRoleMma, stage, tile);
-            ok = false;
-            break;
+          if (!full_ready) {
+            res = wait_phase(bar_full(ctl, stage), phase, abort_flag, limit, wf);
+            res = __shfl_sync(0xffffffffu, res, 0);
+            if (res != kWaitOk) {
+              if (issuer) record_failure(p, abort_flag, res, kRoleMma, stage, tile);
+              ok = false;
+              break;
+            }
           }
           ptx::tc_fence_after();
           if (it == 0 && kb == kb0) trace(p, 4);
           const uint32_t a_addr = a0 + (uint32_t)stage * kASlotBytes;
           const uint32_t b_addr = b0 + (uint32_t)stage * p.b_slot_bytes;
-          const bool store_kb = store && kb >= st_lo && kb < st_hi;
+          const int next_stage = (stage + 1 == S) ? 0 : stage + 1;
+          const uint32_t next_phase = (stage + 1 == S) ? (phase ^ 1u) : phase;
+          full_ready = kb + 1 < kb1 && ptx::mbar_test_wait(bar_full(ctl, next_stage), next_phase);
+          const bool store_kb = store && kb >= st_lo && kb < st_hi && issuer;
           if (store_kb) {
             // The landed X boxes go out to the gathered LHS as they are; the
             // per-shard maps clip a box at its shard's last row.
@@ -716,54 +739,62 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             ptx::bulk_commit();
             stored_any = true;
           }
+          // K-major operand: the 16-element k step moves 32 bytes inside the
+          // 128-byte swizzle row; MN-major operand: it moves 16 rows of 128 B.
+          // A descriptor's address field counts 16-byte units.
+          const uint64_t a_desc0 =
+              a_mn ? ptx::smem_desc_sw128(a_addr, 8192u, 1024u) : ptx::smem_desc_sw128(a_addr, 16u, 1024u);
+          const uint64_t b_desc0 =
+              b_mn ? ptx::smem_desc_sw128(b_addr, 8192u, 1024u) : ptx::smem_desc_sw128(b_addr, 16u, 1024u);
+          const uint64_t a_step = a_mn ? 2048u / 16u : 32u / 16u;
+          const uint64_t b_step = b_mn ? 2048u / 16u : 32u / 16u;
+          if (issuer) {
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk) {
-            // K-major operand: the 16-element k step moves 32 bytes inside the
-            // 128-byte swizzle row; MN-major operand: it moves 16 rows of 128 B.
-            const uint64_t a_desc =
-                a_mn ? ptx::smem_desc_sw128(a_addr + kk * 2048u, 8192u, 1024u)
-                     : ptx::smem_desc_sw128(a_addr + kk * 32u, 16u, 1024u);
-            const uint64_t b_desc =
-                b_mn ? ptx::smem_desc_sw128(b_addr + kk * 2048u, 8192u, 1024u)
-                     : ptx::smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
+            for (int kk = 0; kk < kTileK / 16; ++kk) {
+              const uint64_t a_desc = a_desc0 + a_step * (uint64_t)kk;
+              const uint64_t b_desc = b_desc0 + b_step * (uint64_t)kk;
+              if constexpr (kPair)
+                ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+              else
+                ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            }
+            // the stores must have read the stage before it is released
+            if (store_kb) ptx::bulk_wait_read_all();
+            // frees the stage (in every cluster CTA: their producers multicast
+            // into it) once these MMAs finish
             if constexpr (kPair)
-              ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+              ptx::mma_commit_pair(bar_empty(ctl, stage), kPairMask);
+            else if constexpr (kCM > 1)
+              ptx::mma_commit_multicast(bar_empty(ctl, stage), cmask);
             else
-              ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+              ptx::mma_commit(bar_empty(ctl, stage));
           }
-          // the stores must have read the stage before it is released
-          if (store_kb) ptx::bulk_wait_read_all();
-          // frees the stage (in every cluster CTA: their producers multicast
-          // into it) once these MMAs finish
-          if constexpr (kPair)
-            ptx::mma_commit_pair(bar_empty(ctl, stage), kPairMask);
-          else if constexpr (kCM > 1)
-            ptx::mma_commit_multicast(bar_empty(ctl, stage), cmask);
-          else
-            ptx::mma_commit(bar_empty(ctl, stage));
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          stage = next_stage;
+          phase = next_phase;
         }
         if (!ok) break;
         // accumulator ready for the epilogue (of both CTAs of a pair)
-        if constexpr (kPair)
-          ptx::mma_commit_pair(bar_acc_full(ctl, acc), kPairMask);
-        else
-          ptx::mma_commit(bar_acc_full(ctl, acc));
+        if (issuer) {
+          if constexpr (kPair)
+            ptx::mma_commit_pair(bar_acc_full(ctl, acc), kPairMask);
+          else
+            ptx::mma_commit(bar_acc_full(ctl, acc));
+        }
       }
-      if (stored_any) ptx::bulk_wait_all();
+      if (issuer) {
+        if (stored_any) ptx::bulk_wait_all();
+        trace_value(p, 14, waited_full);
+        trace_value(p, 15, waited_accfree);
+        // Every MMA this thread issued has finished once the drain barrier fires.
+        if constexpr (kPair)
+          ptx::mma_commit_pair(bar_drain(ctl), kPairMask);
+        else
+          ptx::mma_commit(bar_drain(ctl));
+        if (!wait_drain(bar_drain(ctl), 0, limit))
+          record_failure(p, abort_flag, kWaitTimeout, kRoleDrain, -1, -1);
+      }
       trace(p, 5);
-      trace_value(p, 14, waited_full);
-      trace_value(p, 15, waited_accfree);
-      // Every MMA this thread issued has finished once the drain barrier fires.
-      if constexpr (kPair)
-        ptx::mma_commit_pair(bar_drain(ctl), kPairMask);
-      else
-        ptx::mma_commit(bar_drain(ctl));
-      if (!wait_drain(bar_drain(ctl), 0, limit))
-        record_failure(p, abort_flag, kWaitTimeout, kRoleDrain, -1, -1);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ epilogue
