@@ -154,6 +154,8 @@ struct agmm_plan_s {
   const void* cache_xcat = nullptr;  // buffer the gathered-LHS maps describe
   KernelParams params{};
   agmm_plan_s* sub = nullptr;  // unfused path: P = 1 over the gathered buffer
+  agmm_plan_s* gather = nullptr;  // CTA-pair plans: the same tiles without the pair, for agmm_run_gather
+  agmm_tile_config_t user_cfg{};  // the caller's configuration (fields 0 when none)
   size_t out_elem = 2;
   int64_t M() const { return (int64_t)P * m_pd; }
 };
@@ -456,14 +458,14 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
     // TMA multicast (each loads half), cutting per-SM operand traffic by a third.
     const int cm = c.cluster_m ? c.cluster_m : (pl->num_m_tiles >= 2 ? 2 : 1);
     pl->key.cm = cm;
-    // Two-CTA clusters either multiply alone with the Y tile multicast (the
-    // default) or, with cta_pair on, as a cta_group::2 pair in which each CTA
-    // holds its 128 rows and half the Y tile (32 KiB per k block and SM instead
-    // of 48 KiB).  On GB300 the pair measured no faster for Y stored [n, k] and
-    // slower for Y stored [k, n], so it stays opt-in.
+    // Two-CTA clusters multiply as a cta_group::2 pair (the default): each CTA
+    // holds its 128 rows and half the Y tile, 32 KiB per k block and SM, and
+    // reads half the Y operand per MMA.  With cta_pair off each CTA multiplies
+    // alone and the Y tile is multicast (48 KiB per k block and SM).  The pair
+    // measured 4-10 % faster on every row-tile workload, in both Y layouts.
     if (c.cta_pair == AGMM_CFG_ON && cm != 2 && strict.cta_pair == AGMM_CFG_ON)
       return fail(AGMM_ERR_UNSUPPORTED, "config.cta_pair needs cluster_m 2");
-    pl->key.pair = cm == 2 && c.cta_pair == AGMM_CFG_ON;
+    pl->key.pair = cm == 2 && c.cta_pair != AGMM_CFG_OFF;
     pl->num_mc_tiles = (pl->num_m_tiles + cm - 1) / cm;
     if ((int64_t)pl->num_mc_tiles * pl->num_n_tiles > ((int64_t)1 << 31) - 1)
       return fail(AGMM_ERR_INVALID_ARG, "too many output tiles");
@@ -646,9 +648,20 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   kp.pdl = env_int("AGMM_PDL", 1) != 0;
   kp.f16 = pl->f16 ? 1 : 0;
   kp.dp_tiles = pl->dp_tiles;
+  if (config) pl->user_cfg = *config;
   if (with_sub && P > 1) {
     st = plan_impl(1, pl->M(), k, n, dtype, rhs_t, nullptr, false, &pl->sub);
     if (st != AGMM_OK) {
+      delete pl;
+      return st;
+    }
+  }
+  if (with_sub && pl->key.pair) {
+    agmm_tile_config_t gc = pl->user_cfg;
+    gc.cta_pair = AGMM_CFG_OFF;
+    st = plan_impl(P, m_pd, k, n, dtype, rhs_t, &gc, false, &pl->gather);
+    if (st != AGMM_OK) {
+      agmm_destroy(pl->sub);
       delete pl;
       return st;
     }
@@ -822,12 +835,14 @@ agmm_status_t agmm_plan(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_
 void agmm_destroy(agmm_plan_t plan) {
   if (!plan) return;
   agmm_destroy(plan->sub);
+  agmm_destroy(plan->gather);
   delete plan;
 }
 
 size_t agmm_workspace_bytes(agmm_plan_t plan, int unfused) {
   if (!plan) return 0;
-  if (!unfused || plan->P == 1) return kStatusBytes + plan->tail_bytes;
+  if (!unfused || plan->P == 1)
+    return kStatusBytes + std::max(plan->tail_bytes, plan->gather ? plan->gather->tail_bytes : (size_t)0);
   return kStatusBytes + gathered_bytes(plan) + plan->sub->tail_bytes;
 }
 
@@ -845,8 +860,6 @@ agmm_status_t agmm_run_gather(agmm_plan_t plan, const void* const* x_shards, con
   if (st != AGMM_OK) return st;
   if (!xcat) return fail(AGMM_ERR_INVALID_ARG, "xcat is NULL");
   if (!aligned16(xcat)) return fail(AGMM_ERR_ALIGNMENT, "xcat must be 16-byte aligned");
-  if (plan->key.pair)
-    return fail(AGMM_ERR_UNSUPPORTED, "the CTA-pair row kernel does not store the gathered LHS (unset AGMM_PAIR)");
   const size_t gbytes = (size_t)plan->M() * plan->k * 2;
   const size_t xbytes = (size_t)plan->m_pd * plan->k * 2;
   for (int r = 0; r < plan->P; ++r)
@@ -855,7 +868,11 @@ agmm_status_t agmm_run_gather(agmm_plan_t plan, const void* const* x_shards, con
       overlaps(o, (size_t)plan->M() * plan->n * plan->out_elem, xcat, gbytes) ||
       overlaps(workspace, agmm_workspace_bytes(plan, 0), xcat, gbytes))
     return fail(AGMM_ERR_INVALID_ARG, "xcat overlaps Y, O or the workspace");
-  return launch_fused(plan, x_shards, y, o, my_id, workspace, static_cast<uint8_t*>(workspace) + kStatusBytes,
+  // the CTA-pair kernel does not store X boxes: run the plan's companion
+  agmm_plan_s* run = plan->key.pair ? plan->gather : plan;
+  if (!run) return fail(AGMM_ERR_UNSUPPORTED, "no plan without the CTA pair for the gathered LHS");
+  run->params.trace = plan->params.trace;
+  return launch_fused(run, x_shards, y, o, my_id, workspace, static_cast<uint8_t*>(workspace) + kStatusBytes,
                       static_cast<cudaStream_t>(stream), xcat);
 }
 
@@ -930,7 +947,9 @@ agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream)
 
 size_t agmm_trace_bytes(agmm_plan_t plan) {
   if (!plan) return 0;
-  return (size_t)plan->grid.x * plan->grid.y * plan->grid.z * kTraceSlots * sizeof(uint64_t);
+  size_t ctas = (size_t)plan->grid.x * plan->grid.y * plan->grid.z;
+  if (plan->gather) ctas = std::max(ctas, (size_t)plan->gather->grid.x * plan->gather->grid.y * plan->gather->grid.z);
+  return ctas * kTraceSlots * sizeof(uint64_t);
 }
 
 agmm_status_t agmm_set_trace(agmm_plan_t plan, void* trace, size_t bytes) {

@@ -344,10 +344,10 @@ def bench_ours(args, w):
     del g2
 
     # the fused path that also writes the gathered LHS (what the unfused path
-    # materialises too): one gathered buffer per replica, same method
-    # (the opt-in CTA-pair row kernel does not store it: no entry then)
+    # materialises too): one gathered buffer per replica, same method (a
+    # CTA-pair plan runs it through its companion plan without the pair)
     gath_ms = None
-    if os.environ.get("AGMM_PAIR", "0") in ("", "0"):
+    if True:
         xcats = [torch.empty((w.M, w.k), dtype=r[2].dtype, device=device) for r in reps]
         torch.cuda.synchronize()
         gath = [(lambda rep, xc: (lambda s: plan.run_gather(rep[0], rep[1], rep[2], xc, w.my_id, ws, s)))(r, xc)

@@ -213,8 +213,10 @@ agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void
  * that load it: n tile t stores the k blocks in the t-th share of the k
  * range, so the gathered rows are written once, never read back, and the
  * store work is spread over all n tiles.  xcat must not overlap the shards, Y, O or the workspace
- * (AGMM_ERR_INVALID_ARG).  Plans of the opt-in CTA-pair row kernel
- * (AGMM_PAIR=1) return AGMM_ERR_UNSUPPORTED.
+ * (AGMM_ERR_INVALID_ARG).  The CTA-pair row kernel does not store the
+ * gathered rows: a plan that uses it runs this call through a companion plan
+ * of the same tiles without the pair (built with the plan, covered by
+ * agmm_workspace_bytes(plan, 0)).
  */
 agmm_status_t agmm_run_gather(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o, void* xcat,
                               int my_id, void* workspace, void* stream);

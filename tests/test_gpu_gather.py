@@ -111,7 +111,7 @@ def test_all_gather_matmul_returns_gathered(agmm):
     check(o, ref32, "all_gather_matmul return_gathered")
 
 
-def test_gathered_lhs_argument_errors(agmm, monkeypatch):
+def test_gathered_lhs_argument_errors_and_pair_plans(agmm):
     P, m, k, n = 2, 16, 256, 128
     xs_cpu, y_cpu = make_inputs(P, m, k, n, False, seed=16)
     xs = [x.cuda() for x in xs_cpu]
@@ -124,18 +124,19 @@ def test_gathered_lhs_argument_errors(agmm, monkeypatch):
     with pytest.raises(agmm.AgmmError) as err:
         plan.run_gather(xs, y, o, xs[0], 0, ws)
     assert err.value.status == agmm.AGMM_ERR_INVALID_ARG
-    # the CTA-pair row kernel does not store it
-    monkeypatch.setenv("AGMM_PAIR", "1")
-    monkeypatch.setenv("AGMM_PATH", "0")
-    monkeypatch.setenv("AGMM_CM", "2")
+    # a CTA-pair plan (the row-tile default for two-CTA clusters) runs this
+    # call through its companion plan without the pair
     pm, pk, pn = 256, 512, 256
     xs2, y2 = make_inputs(2, pm, pk, pn, False, seed=17)
-    pplan = agmm.Plan(2, pm, pk, pn, False)
-    if pplan.info()["path"] == 0:
-        o2 = torch.empty((2 * pm, pn), dtype=torch.bfloat16, device="cuda")
-        xc = torch.empty((2 * pm, pk), dtype=torch.bfloat16, device="cuda")
-        ws2 = pplan.new_workspace()
-        torch.cuda.synchronize()
-        with pytest.raises(agmm.AgmmError) as err:
-            pplan.run_gather([x.cuda() for x in xs2], y2.cuda(), o2, xc, 0, ws2)
-        assert err.value.status == agmm.AGMM_ERR_UNSUPPORTED
+    pplan = agmm.Plan(2, pm, pk, pn, False, config={"path": "rows", "cluster_m": 2, "cta_pair": True})
+    assert pplan.info()["cta_pair"] == 1
+    o2 = torch.empty((2 * pm, pn), dtype=torch.bfloat16, device="cuda")
+    xc = torch.empty((2 * pm, pk), dtype=torch.bfloat16, device="cuda")
+    ws2 = pplan.new_workspace()
+    torch.cuda.synchronize()
+    pplan.run_gather([x.cuda() for x in xs2], y2.cuda(), o2, xc, 0, ws2)
+    pplan.query_status(ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(xc.cpu().view(torch.int16), torch.cat(xs2).view(torch.int16))
+    ref32, _ = oracle.agmm(xs2, y2, False)
+    check(o2, ref32, "CTA-pair plan with gathered LHS")
