@@ -503,14 +503,26 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           swap_pending = false;
           bytes = (uint32_t)kASlotBytes + (uint32_t)swap_nch * p.box_rows * 128u;
         }
+        // One X box per stage (the usual row tile of one 128-row chunk) is
+        // kept in registers rather than the chunk arrays.
+        const CUtensorMap* xmap0 = (kPath == kPathRows && nchunks > 0) ? &p.xmap[shard_j[0]] : nullptr;
+        const int xrow0 = (kPath == kPathRows && nchunks > 0) ? row_j[0] : 0;
+        // The next stage's empty barrier is tested while this stage's copies
+        // are issued, so its latency is off the loop's critical path.
+        bool empty_ready = false;
         for (int kb = kb0; kb < kb1; ++kb) {
-          int res = wait_phase(bar_empty(ctl, stage), phase ^ 1u, abort_flag, limit, wait_acc);
-          res = __shfl_sync(0xffffffffu, res, 0);
-          if (res != kWaitOk) {
-            if (leader) record_failure(p, abort_flag, res, kRoleProducer, stage, tile);
-            ok = false;
-            break;
+          if (!empty_ready) {
+            int res = wait_phase(bar_empty(ctl, stage), phase ^ 1u, abort_flag, limit, wait_acc);
+            res = __shfl_sync(0xffffffffu, res, 0);
+            if (res != kWaitOk) {
+              if (leader) record_failure(p, abort_flag, res, kRoleProducer, stage, tile);
+              ok = false;
+              break;
+            }
           }
+          const int next_stage = (stage + 1 == S) ? 0 : stage + 1;
+          const uint32_t next_phase = (stage + 1 == S) ? (phase ^ 1u) : phase;
+          empty_ready = kb + 1 < kb1 && ptx::mbar_test_wait(bar_empty(ctl, next_stage), next_phase ^ 1u);
           // A pair follower's copies complete on the leader's barrier.
           const bool to_leader = kPair && crank == 1;
           const uint32_t full = to_leader ? ptx::map_shared_rank(bar_full(ctl, stage), 0) : bar_full(ctl, stage);
@@ -531,13 +543,20 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             const uint32_t b_dst = b0 + (uint32_t)stage * p.b_slot_bytes;
             const int k0 = kb * kTileK;
             if constexpr (kPath == kPathRows) {
-              for (int j = 0; j < nchunks; ++j) {
+              if (nchunks == 1) {
                 if (to_leader)
-                  ptx::tma_load_2d_pair(a_dst + (uint32_t)j * p.box_rows * 128u, &p.xmap[shard_j[j]], full, k0,
-                                        row_j[j]);
+                  ptx::tma_load_2d_pair(a_dst, xmap0, full, k0, xrow0);
                 else
-                  ptx::tma_load_2d(a_dst + (uint32_t)j * p.box_rows * 128u, &p.xmap[shard_j[j]], full, k0,
-                                   row_j[j]);
+                  ptx::tma_load_2d(a_dst, xmap0, full, k0, xrow0);
+              } else {
+                for (int j = 0; j < nchunks; ++j) {
+                  if (to_leader)
+                    ptx::tma_load_2d_pair(a_dst + (uint32_t)j * p.box_rows * 128u, &p.xmap[shard_j[j]], full, k0,
+                                          row_j[j]);
+                  else
+                    ptx::tma_load_2d(a_dst + (uint32_t)j * p.box_rows * 128u, &p.xmap[shard_j[j]], full, k0,
+                                     row_j[j]);
+                }
               }
               if constexpr (kCM == 1) {
                 if constexpr (kYK) {
@@ -615,10 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             trace(p, 2);
             traced_first = true;
           }
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          stage = next_stage;
+          phase = next_phase;
         }
       }
       trace(p, 3);
