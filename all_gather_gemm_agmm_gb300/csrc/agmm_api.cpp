@@ -441,7 +441,17 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
         }
       }
     if (tiles_best > (int64_t)1 << 30) return fail(AGMM_ERR_INVALID_ARG, "too many row tiles");
+    // Clusters of two CTAs on neighbouring row tiles share each Y tile
+    // (below: as a CTA pair, or through TMA multicast).
+    const int cm = c.cluster_m ? c.cluster_m : (tiles_best >= 2 ? 2 : 1);
+    // 256-wide tiles, unless they would not give half the clusters a whole
+    // tile (stream-K then splits most of the work): 128-wide tiles double
+    // the tile count.
     int bn = (pl->n % 256 == 0) ? 256 : 128;
+    if (bn == 256) {
+      const int64_t tiles256 = (tiles_best + cm - 1) / cm * (pl->n / 256);
+      if (2 * tiles256 < pl->num_sms / cm) bn = 128;
+    }
     if (c.tile_n) {
       if (pl->n % c.tile_n == 0)
         bn = c.tile_n;
@@ -454,9 +464,6 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
     pl->total_chunks = (int)ring_total_chunks(make_ring_geom(pl->P, pl->m_pd, 0, bh_best, whole_best));
     pl->num_m_tiles = (int)tiles_best;
     pl->num_n_tiles = (int)(pl->n / bn);
-    // Clusters of two CTAs on neighbouring row tiles share each Y tile through
-    // TMA multicast (each loads half), cutting per-SM operand traffic by a third.
-    const int cm = c.cluster_m ? c.cluster_m : (pl->num_m_tiles >= 2 ? 2 : 1);
     pl->key.cm = cm;
     // Two-CTA clusters multiply as a cta_group::2 pair (the default): each CTA
     // holds its 128 rows and half the Y tile, 32 KiB per k block and SM, and

@@ -36,7 +36,7 @@ PINNED = {
     "c4_prefill": (0, 128, 0, 128, 256, 7, 1, 1),
     "sweep_P8_m8_nt": (1, 8, 1, 8, 64, 8, 1, 7),
     "sweep_P2_m1000_nt": (0, 128, 0, 16, 256, 7, 1, 1),
-    "sweep_P4_m128_rt": (0, 128, 1, 4, 256, 7, 1, 1),
+    "sweep_P4_m128_rt": (0, 128, 1, 4, 128, 8, 1, 1),  # 128-wide: 256-wide gives 20 cluster tiles
 }
 
 
