@@ -5,20 +5,29 @@
 //   _do_o_local_copy for the output row placement)
 //
 // One warp-specialised CTA of 6 warps:
-//   warp 0      one elected thread issues TMA loads of X chunks (through the
-//               per-shard tensor-map table, in ring order) and Y tiles into a
-//               multi-stage shared-memory ring guarded by full/empty mbarriers;
-//   warp 1      allocates tensor memory; one thread issues tcgen05.mma
-//               (bf16 x bf16 or fp16 x fp16 -> f32 accumulators in TMEM) and
-//               tcgen05.commit; optionally it also TMA-stores the landed X
-//               boxes to a gathered-LHS buffer before releasing each stage;
+//   warp 0      runs the load loop converged; one elected lane issues TMA
+//               loads of X chunks (through the per-shard tensor-map table, in
+//               ring order) and Y tiles into a multi-stage shared-memory ring
+//               guarded by full/empty mbarriers;
+//   warp 1      allocates tensor memory and runs the MMA loop converged; one
+//               elected lane issues tcgen05.mma (bf16 x bf16 or fp16 x fp16 ->
+//               f32 accumulators in TMEM) and tcgen05.commit; optionally it
+//               also TMA-stores the landed X boxes to a gathered-LHS buffer
+//               before releasing each stage;
 //   warps 2-5   drain TMEM with tcgen05.ld, round to the output dtype and store
 //               each row at its rank-order offset.
+// Issuing from converged warps keeps the copy and MMA operands warp-uniform;
+// a loop that a single lane runs alone pays for moving them to uniform
+// registers at every issue.  Both loops test the next stage's barrier while
+// they issue the current stage.
 //
 // Two tile orientations:
-//   rows path  MMA M = 128 gathered rows (ring-ordered chunks), MMA N = n tile;
-//              persistent CTAs walk the tile list, TMEM holds two accumulators
-//              so the epilogue of one tile overlaps the main loop of the next.
+//   rows path  MMA M = 128 gathered rows (ring-ordered chunks) per CTA, MMA
+//              N = n tile; clusters of two CTAs multiply as a cta_group::2
+//              pair (each CTA holding half the Y tile) or alone with the Y
+//              tile multicast; persistent clusters walk the tile list, TMEM
+//              holds two accumulators so the epilogue of one tile overlaps the
+//              main loop of the next.
 //   swap path  (the whole gathered LHS fits in one MMA N <= 256) MMA M = 128
 //              columns of n, MMA N = the gathered rows of one row group; k is
 //              split across the CTAs of a thread-block cluster and the float32
