@@ -179,3 +179,38 @@ def test_candidates_are_distinct_and_start_with_the_rules():
         keys = {tune._plan_key(agmm.plan_preview(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, num_sms=SMS,
                                                  config=c)) for c in cands}
         assert len(keys) == len(cands) > 3, name
+
+
+def test_random_configs_plan_or_fail_cleanly():
+    # any combination of fields either plans (and the plan keeps the planner's
+    # invariants) or fails with a status, on random shapes
+    import numpy as np
+
+    rng = np.random.default_rng(99)
+    choices = {
+        "path": [0, 1, 2, "rows", "swap"], "chunks": [0, 1, 2], "box_rows": [0, 8, 16, 32, 64, 128],
+        "tile_n": [0, 128, 256], "cluster_m": [0, 1, 2], "cta_pair": [None, True, False], "stages": [0, 2, 3, 5, 8],
+        "group_m": [0, 1, 3, 8, 64], "stream_k": [None, True, False], "row_groups": [0, 1, 2, 4, 8],
+        "splits": [0, 1, 2, 5, 16], "dsmem_reduce": [None, True, False], "tuned_table": [None, True, False],
+    }
+    planned = 0
+    for _ in range(600):
+        P = int(rng.integers(1, 9))
+        m = int(rng.choice([1, 7, 16, 64, 100, 256, 1000]))
+        k = 128 * int(rng.integers(1, 40))
+        n = 128 * int(rng.integers(1, 30))
+        cfg = {f: v[int(rng.integers(0, len(v)))] for f, v in choices.items() if rng.random() < 0.4}
+        try:
+            info = agmm.plan_preview(P, m, k, n, bool(rng.integers(0, 2)), num_sms=SMS, config=cfg)
+        except agmm.AgmmError as e:
+            assert e.status in (agmm.AGMM_ERR_INVALID_ARG, agmm.AGMM_ERR_UNSUPPORTED), (cfg, e)
+            continue
+        planned += 1
+        assert 2 <= info["stages"] <= 8 and info["smem_bytes"] <= 232448, (cfg, info)
+        assert info["box_rows"] in (8, 16, 32, 64, 128), (cfg, info)
+        if info["path"] == 0:
+            assert info["tile_n"] in (128, 256) and n % info["tile_n"] == 0, (cfg, info)
+            assert info["cta_pair"] in (0, 1) and (info["cta_pair"] == 0 or info["cluster_m"] == 2), (cfg, info)
+        else:
+            assert info["tile_n"] <= 256 and 1 <= info["splits"] <= 16, (cfg, info)
+    assert planned > 200
