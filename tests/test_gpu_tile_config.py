@@ -91,3 +91,45 @@ def test_infeasible_config_fails_before_launch(agmm):
     with pytest.raises(agmm.AgmmError) as err:
         agmm.Plan(8, 64, 512, 256, False, config={"path": "swap"})
     assert err.value.status == agmm.AGMM_ERR_UNSUPPORTED
+
+
+def test_random_configs_match_oracle(agmm):
+    # seeded random (shape, configuration) pairs the planner accepts: every
+    # one meets the parity gate, with nothing stored outside O
+    import numpy as np
+
+    rng = np.random.default_rng(123)
+    choices = {
+        "path": ["rows", "swap"], "chunks": ["half", "whole"], "box_rows": [8, 16, 32, 64, 128],
+        "tile_n": [128, 256], "cluster_m": [1, 2], "cta_pair": [True, False], "stages": [2, 3, 8],
+        "group_m": [1, 3, 8], "stream_k": [True, False], "row_groups": [1, 2, 4], "splits": [1, 2, 3, 6],
+        "dsmem_reduce": [True, False],
+    }
+    ran = 0
+    for trial in range(40):
+        P = int(rng.integers(1, 6))
+        m = int(rng.choice([5, 16, 40, 77, 130]))
+        k = 128 * int(rng.integers(1, 6))
+        n = 256 * int(rng.integers(1, 3))
+        rt = bool(rng.integers(0, 2))
+        cfg = {f: v[int(rng.integers(0, len(v)))] for f, v in choices.items() if rng.random() < 0.5}
+        cfg["tuned_table"] = False
+        try:
+            agmm.plan_preview(P, m, k, n, rt, config=cfg)
+        except agmm.AgmmError:
+            continue  # a combination this shape cannot hold
+        xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=200 + trial)
+        ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+        xs = [to_device_guarded(x)[0] for x in xs_cpu]
+        y, _ = to_device_guarded(y_cpu)
+        o, obuf = alloc_output_guarded(P * m, n)
+        plan = agmm.Plan(P, m, k, n, rt, config=cfg)
+        ws = plan.new_workspace()
+        torch.cuda.synchronize()
+        plan.run(xs, y, o, int(rng.integers(0, P)), ws)
+        plan.query_status(ws)
+        torch.cuda.synchronize()
+        assert guards_intact(obuf), (P, m, k, n, rt, cfg)
+        check(o, ref32, f"{(P, m, k, n, rt)} {cfg} {plan.info()}")
+        ran += 1
+    assert ran >= 15
