@@ -134,6 +134,7 @@ struct agmm_plan_s {
   int box_rows = 0, total_chunks = 0, num_m_tiles = 0, num_mc_tiles = 0, num_n_tiles = 0, num_k_blocks = 0;
   int group_m = 1, num_tiles = 0, stages = 0, mma_n = 0, tmem_cols = 0, splits = 1;
   uint32_t b_slot_bytes = 0;
+  int atoms = 1;  // k blocks per pipeline stage (swapped tiles: 1 or 2)
   size_t smem_bytes = 0;
   dim3 grid{1, 1, 1};
   int cluster_x = 1;
@@ -404,7 +405,12 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
     pl->group_chunks = (pl->total_chunks + best_g - 1) / best_g;
     pl->mma_n = (pl->group_chunks * pl->box_rows + 31) / 32 * 32;
     pl->b_slot_bytes = (uint32_t)pl->mma_n * 128u;
-    const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
+    // Two k blocks per stage halve the barrier hand-offs per block, as long
+    // as at least three stages still fit (MMA N <= 128); wider tiles keep
+    // one block per stage and their deeper ring.
+    pl->atoms = budget / (2 * (kASlotBytes + (int64_t)pl->b_slot_bytes)) >= 3 ? 2 : 1;
+    pl->key.atoms = pl->atoms;
+    const int64_t stage_bytes = (kASlotBytes + pl->b_slot_bytes) * pl->atoms;
     pl->stages = (int)std::min<int64_t>(kMaxStages, budget / stage_bytes);
     if (c.stages) pl->stages = std::min(pl->stages, c.stages);
     // The k splits (cluster size); plan_impl lowers them until one wave of
@@ -487,7 +493,7 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
     pl->group_m = c.group_m ? c.group_m : 8;
     pl->stream_k = c.stream_k != AGMM_CFG_OFF;
   }
-  pl->smem_bytes = tmem_safe_smem(1024 + (size_t)pl->stages * (kASlotBytes + pl->b_slot_bytes) + kCtlBytes,
+  pl->smem_bytes = tmem_safe_smem(1024 + (size_t)pl->stages * (kASlotBytes + pl->b_slot_bytes) * pl->atoms + kCtlBytes,
                                   pl->tmem_cols);
   return AGMM_OK;
 }
@@ -573,7 +579,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
     if (pl->key.path == kPathSwap) {
       // The k-split reduction reuses the pipeline slots as its receive buffer:
       // splits x cpo slots of 128 floats (cpo = owner columns, 16-aligned).
-      const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
+      const int64_t stage_bytes = (kASlotBytes + pl->b_slot_bytes) * pl->atoms;
       const int64_t budget = (int64_t)kMaxDynSmem - 1024 - kCtlBytes;
       const int64_t groups = (pl->group_chunks * (int64_t)pl->box_rows + 15) / 16;
       const int64_t cpo = (groups + pl->splits - 1) / pl->splits * 16;

@@ -357,10 +357,11 @@ __device__ __forceinline__ void owner_sum_global(const KernelParams& p, const Ow
 // (K-major tiles); otherwise Y is [k, n] and its tiles are MN-major.  kF32:
 // float32 output.  kBN: n tile of the rows path (the swap path uses 128).
 // ----------------------------------------------------------------------------
-template <int kPath, bool kYK, bool kF32, int kBN, int kCM, bool kPair>
+template <int kPath, bool kYK, bool kF32, int kBN, int kCM, bool kPair, int kAtoms>
 __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_constant__ KernelParams p) {
   static_assert(kCM == 1 || (kPath == kPathRows && (kYK || kBN / 64 >= kCM)), "bad cluster multicast shape");
   static_assert(!kPair || (kCM == 2 && kPath == kPathRows), "CTA pairs are clusters of two on the rows path");
+  static_assert(kAtoms == 1 || (kAtoms == 2 && kPath == kPathSwap), "two k blocks per stage: swapped tiles");
   // The leader's accumulator-release barrier receives the follower's
   // epilogue arrivals (release at cluster scope): its wait acquires at
   // cluster scope.  Stage barriers are fed by TMA and tcgen05.commit.
@@ -370,9 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
   const int S = p.stages;
+  // A stage holds `A` k blocks, each laid out as a one-block stage.  Swapped
+  // tiles of MMA N <= 128 take two per stage, so the producer and the MMA
+  // issuer hand off once per two blocks (their barrier operations cost as
+  // much as a block's MMAs at these tile sizes).
+  constexpr int A = kAtoms;
+  const uint32_t a_slot = (uint32_t)A * kASlotBytes;
+  const uint32_t b_slot = (uint32_t)A * p.b_slot_bytes;
   const uint32_t a0 = base;
-  const uint32_t b0 = base + (uint32_t)S * kASlotBytes;
-  const uint32_t ctl = b0 + (uint32_t)S * p.b_slot_bytes;
+  const uint32_t b0 = base + (uint32_t)S * a_slot;
+  const uint32_t ctl = b0 + (uint32_t)S * b_slot;
   uint8_t* ctl_ptr = base_ptr + (ctl - base);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl_ptr + kAbortOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl_ptr + kTmemOffset);
@@ -519,7 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         // The next stage's empty barrier is tested while this stage's copies
         // are issued, so its latency is off the loop's critical path.
         bool empty_ready = false;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += A) {
+          const int na = min(A, kb1 - kb);  // k blocks in this stage
           if (!empty_ready) {
             int res = wait_phase(bar_empty(ctl, stage), phase ^ 1u, abort_flag, limit, wait_acc);
             res = __shfl_sync(0xffffffffu, res, 0);
@@ -531,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           }
           const int next_stage = (stage + 1 == S) ? 0 : stage + 1;
           const uint32_t next_phase = (stage + 1 == S) ? (phase ^ 1u) : phase;
-          empty_ready = kb + 1 < kb1 && ptx::mbar_test_wait(bar_empty(ctl, next_stage), next_phase ^ 1u);
+          empty_ready = kb + A < kb1 && ptx::mbar_test_wait(bar_empty(ctl, next_stage), next_phase ^ 1u);
           // A pair follower's copies complete on the leader's barrier.
           const bool to_leader = kPair && crank == 1;
           const uint32_t full = to_leader ? ptx::map_shared_rank(bar_full(ctl, stage), 0) : bar_full(ctl, stage);
@@ -545,12 +554,17 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           }
           if (!drop && leader) {
             if (to_leader)
-              ptx::mbar_arrive_expect_tx_remote(full, bytes);
+              ptx::mbar_arrive_expect_tx_remote(full, bytes * (uint32_t)na);
             else
-              ptx::mbar_arrive_expect_tx(full, bytes);
-            const uint32_t a_dst = a0 + (uint32_t)stage * kASlotBytes;
-            const uint32_t b_dst = b0 + (uint32_t)stage * p.b_slot_bytes;
-            const int k0 = kb * kTileK;
+              ptx::mbar_arrive_expect_tx(full, bytes * (uint32_t)na);
+            const uint32_t a_dst0 = a0 + (uint32_t)stage * a_slot;
+            const uint32_t b_dst0 = b0 + (uint32_t)stage * b_slot;
+#pragma unroll
+            for (int at = 0; at < A; ++at) {
+            if (at >= na) break;
+            const uint32_t a_dst = a_dst0 + (uint32_t)at * kASlotBytes;
+            const uint32_t b_dst = b_dst0 + (uint32_t)at * p.b_slot_bytes;
+            const int k0 = (kb + at) * kTileK;
             if constexpr (kPath == kPathRows) {
               if (nchunks == 1) {
                 if (to_leader)
@@ -638,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
                 ptx::tma_load_2d(b_dst + (uint32_t)c * chunk_bytes, &p.xmap[e.x], full, k0, e.y);
               }
             }
+            }  // k blocks of the stage
           }
           if (!traced_first) {
             trace(p, 2);
@@ -725,7 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         // The next stage's full barrier is tested while this stage's MMAs
         // are issued, so its latency is off the loop's critical path.
         bool full_ready = false;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += A) {
+          const int na = min(A, kb1 - kb);  // k blocks in this stage
           // (a pair: this barrier also counts the follower's copies)
           if (!full_ready) {
             res = wait_phase(bar_full(ctl, stage), phase, abort_flag, limit, wf);
@@ -738,12 +754,19 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           }
           ptx::tc_fence_after();
           if (it == 0 && kb == kb0) trace(p, 4);
-          const uint32_t a_addr = a0 + (uint32_t)stage * kASlotBytes;
-          const uint32_t b_addr = b0 + (uint32_t)stage * p.b_slot_bytes;
+          const uint32_t a_addr0 = a0 + (uint32_t)stage * a_slot;
+          const uint32_t b_addr0 = b0 + (uint32_t)stage * b_slot;
           const int next_stage = (stage + 1 == S) ? 0 : stage + 1;
           const uint32_t next_phase = (stage + 1 == S) ? (phase ^ 1u) : phase;
-          full_ready = kb + 1 < kb1 && ptx::mbar_test_wait(bar_full(ctl, next_stage), next_phase);
-          const bool store_kb = store && kb >= st_lo && kb < st_hi && issuer;
+          full_ready = kb + A < kb1 && ptx::mbar_test_wait(bar_full(ctl, next_stage), next_phase);
+          bool stored_stage = false;
+#pragma unroll
+          for (int at = 0; at < A; ++at) {
+          if (at >= na) break;
+          const int kbb = kb + at;
+          const uint32_t a_addr = a_addr0 + (uint32_t)at * kASlotBytes;
+          const uint32_t b_addr = b_addr0 + (uint32_t)at * p.b_slot_bytes;
+          const bool store_kb = store && kbb >= st_lo && kbb < st_hi && issuer;
           if (store_kb) {
             // The landed X boxes go out to the gathered LHS as they are; the
             // per-shard maps clip a box at its shard's last row.
@@ -752,18 +775,19 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
                 const int64_t gc = (int64_t)st_mt * cpt + j;
                 if (gc < p.total_chunks) {
                   const RingChunk ch = ring_chunk(geom, gc);
-                  ptx::tma_store_2d(&p.xcatmap[ch.shard], a_addr + (uint32_t)j * chunk_bytes, kb * kTileK,
+                  ptx::tma_store_2d(&p.xcatmap[ch.shard], a_addr + (uint32_t)j * chunk_bytes, kbb * kTileK,
                                     (int)ch.src_row);
                 }
               }
             } else {
               for (int c = 0; c < swap_nch; ++c) {
                 const int4 e = chunk_tab[swap_c0 + c];
-                ptx::tma_store_2d(&p.xcatmap[e.x], b_addr + (uint32_t)c * chunk_bytes, kb * kTileK, e.y);
+                ptx::tma_store_2d(&p.xcatmap[e.x], b_addr + (uint32_t)c * chunk_bytes, kbb * kTileK, e.y);
               }
             }
             ptx::bulk_commit();
             stored_any = true;
+            stored_stage = true;
           }
           // K-major operand: the 16-element k step moves 32 bytes inside the
           // 128-byte swizzle row; MN-major operand: it moves 16 rows of 128 B.
@@ -779,13 +803,17 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
             for (int kk = 0; kk < kTileK / 16; ++kk) {
               const uint64_t a_desc = a_desc0 + a_step * (uint64_t)kk;
               const uint64_t b_desc = b_desc0 + b_step * (uint64_t)kk;
+              const uint32_t accumulate = (kbb > kb0 || kk > 0) ? 1u : 0u;
               if constexpr (kPair)
-                ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, idesc, accumulate);
               else
-                ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, accumulate);
             }
+          }
+          }  // k blocks of the stage
+          if (issuer) {
             // the stores must have read the stage before it is released
-            if (store_kb) ptx::bulk_wait_read_all();
+            if (stored_stage) ptx::bulk_wait_read_all();
             // frees the stage (in every cluster CTA: their producers multicast
             // into it) once these MMAs finish
             if constexpr (kPair)
@@ -1185,23 +1213,26 @@ __global__ void __launch_bounds__(256) agmm_gather_rows(const __grid_constant__ 
 using KernelFn = void (*)(KernelParams);
 
 KernelFn select_kernel(const KernelKey& k) {
-#define AGMM_PICK(PATH, BN, CM, PAIR)                                                        \
-  (k.y_kmajor ? (k.out_f32 ? &agmm_fused_sm103a<PATH, true, true, BN, CM, PAIR>              \
-                           : &agmm_fused_sm103a<PATH, true, false, BN, CM, PAIR>)            \
-              : (k.out_f32 ? &agmm_fused_sm103a<PATH, false, true, BN, CM, PAIR>             \
-                           : &agmm_fused_sm103a<PATH, false, false, BN, CM, PAIR>))
-  if (k.path == kPathSwap) return (k.cm == 1 && !k.pair) ? AGMM_PICK(kPathSwap, 128, 1, false) : nullptr;
+#define AGMM_PICK(PATH, BN, CM, PAIR, AT)                                                    \
+  (k.y_kmajor ? (k.out_f32 ? &agmm_fused_sm103a<PATH, true, true, BN, CM, PAIR, AT>          \
+                           : &agmm_fused_sm103a<PATH, true, false, BN, CM, PAIR, AT>)        \
+              : (k.out_f32 ? &agmm_fused_sm103a<PATH, false, true, BN, CM, PAIR, AT>         \
+                           : &agmm_fused_sm103a<PATH, false, false, BN, CM, PAIR, AT>))
+  if (k.path == kPathSwap) {
+    if (k.cm != 1 || k.pair) return nullptr;
+    return k.atoms == 2 ? AGMM_PICK(kPathSwap, 128, 1, false, 2) : AGMM_PICK(kPathSwap, 128, 1, false, 1);
+  }
   if (k.cm == 1) {
     if (k.pair) return nullptr;
-    if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 1, false);
-    if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 1, false);
+    if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 1, false, 1);
+    if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 1, false, 1);
   } else if (k.cm == 2) {
     if (k.pair) {
-      if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2, true);
-      if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2, true);
+      if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2, true, 1);
+      if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2, true, 1);
     } else {
-      if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2, false);
-      if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2, false);
+      if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2, false, 1);
+      if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2, false, 1);
     }
   }
   return nullptr;
