@@ -447,9 +447,19 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
         }
       }
     if (tiles_best > (int64_t)1 << 30) return fail(AGMM_ERR_INVALID_ARG, "too many row tiles");
-    // Clusters of two CTAs on neighbouring row tiles share each Y tile
-    // (below: as a CTA pair, or through TMA multicast).
-    const int cm = c.cluster_m ? c.cluster_m : (tiles_best >= 2 ? 2 : 1);
+    // Clusters of two CTAs on neighbouring row tiles multiply as a
+    // cta_group::2 pair: each CTA holds its 128 rows and half the Y tile, 32
+    // KiB per k block and SM, and reads half the Y operand per MMA.  No copy
+    // is multicast; a two-CTA cluster is always a pair, so cta_pair off means
+    // one-CTA clusters.
+    int cm = c.cluster_m ? c.cluster_m : (tiles_best >= 2 ? 2 : 1);
+    if (c.cta_pair == AGMM_CFG_ON && cm != 2 && strict.cta_pair == AGMM_CFG_ON)
+      return fail(AGMM_ERR_UNSUPPORTED, "config.cta_pair needs cluster_m 2");
+    if (c.cta_pair == AGMM_CFG_OFF && cm == 2) {
+      if (strict.cta_pair == AGMM_CFG_OFF && strict.cluster_m == 2)
+        return fail(AGMM_ERR_UNSUPPORTED, "a two-CTA cluster multiplies as a CTA pair: cta_pair off needs cluster_m 1");
+      if (strict.cluster_m != 2) cm = 1;
+    }
     // 256-wide tiles, unless they would not give half the clusters a whole
     // tile (stream-K then splits most of the work): 128-wide tiles double
     // the tile count.
@@ -471,14 +481,7 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
     pl->num_m_tiles = (int)tiles_best;
     pl->num_n_tiles = (int)(pl->n / bn);
     pl->key.cm = cm;
-    // Two-CTA clusters multiply as a cta_group::2 pair (the default): each CTA
-    // holds its 128 rows and half the Y tile, 32 KiB per k block and SM, and
-    // reads half the Y operand per MMA.  With cta_pair off each CTA multiplies
-    // alone and the Y tile is multicast (48 KiB per k block and SM).  The pair
-    // measured 4-10 % faster on every row-tile workload, in both Y layouts.
-    if (c.cta_pair == AGMM_CFG_ON && cm != 2 && strict.cta_pair == AGMM_CFG_ON)
-      return fail(AGMM_ERR_UNSUPPORTED, "config.cta_pair needs cluster_m 2");
-    pl->key.pair = cm == 2 && c.cta_pair != AGMM_CFG_OFF;
+    pl->key.pair = cm == 2;
     pl->num_mc_tiles = (pl->num_m_tiles + cm - 1) / cm;
     if ((int64_t)pl->num_mc_tiles * pl->num_n_tiles > ((int64_t)1 << 31) - 1)
       return fail(AGMM_ERR_INVALID_ARG, "too many output tiles");
@@ -672,6 +675,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   if (with_sub && pl->key.pair) {
     agmm_tile_config_t gc = pl->user_cfg;
     gc.cta_pair = AGMM_CFG_OFF;
+    gc.cluster_m = 1;
     st = plan_impl(P, m_pd, k, n, dtype, rhs_t, &gc, false, &pl->gather);
     if (st != AGMM_OK) {
       agmm_destroy(pl->sub);

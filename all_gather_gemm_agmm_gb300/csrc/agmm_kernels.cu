@@ -24,10 +24,10 @@
 // Two tile orientations:
 //   rows path  MMA M = 128 gathered rows (ring-ordered chunks) per CTA, MMA
 //              N = n tile; clusters of two CTAs multiply as a cta_group::2
-//              pair (each CTA holding half the Y tile) or alone with the Y
-//              tile multicast; persistent clusters walk the tile list, TMEM
-//              holds two accumulators so the epilogue of one tile overlaps the
-//              main loop of the next.
+//              pair, each CTA loading and holding half the Y tile (no load is
+//              multicast); persistent clusters walk the tile list, TMEM holds
+//              two accumulators so the epilogue of one tile overlaps the main
+//              loop of the next.
 //   swap path  (the whole gathered LHS fits in one MMA N <= 256) MMA M = 128
 //              columns of n, MMA N = the gathered rows of one row group; k is
 //              split across the CTAs of a thread-block cluster and the float32
@@ -359,7 +359,8 @@ __device__ __forceinline__ void owner_sum_global(const KernelParams& p, const Ow
 // ----------------------------------------------------------------------------
 template <int kPath, bool kYK, bool kF32, int kBN, int kCM, bool kPair, int kAtoms>
 __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_constant__ KernelParams p) {
-  static_assert(kCM == 1 || (kPath == kPathRows && (kYK || kBN / 64 >= kCM)), "bad cluster multicast shape");
+  // Clusters exist only as CTA pairs of the rows path: no copy is multicast.
+  static_assert(kCM == 1 || (kCM == 2 && kPair), "two-CTA clusters multiply as a CTA pair");
   static_assert(!kPair || (kCM == 2 && kPath == kPathRows), "CTA pairs are clusters of two on the rows path");
   static_assert(kAtoms == 1 || (kAtoms == 2 && kPath == kPathSwap), "two k blocks per stage: swapped tiles");
   // The leader's accumulator-release barrier receives the follower's
@@ -399,8 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     for (int s = 0; s < S; ++s) {
       // a pair: both producers count their bytes on the leader's barrier
       ptx::mbar_init(bar_full(ctl, s), kPair ? 2 : 1);
-      // every cluster CTA's MMA frees the stage (a pair: the leader's MMA alone)
-      ptx::mbar_init(bar_empty(ctl, s), kPair ? 1 : kCM);
+      // the MMA frees the stage (a pair: the leader's MMA, for both CTAs)
+      ptx::mbar_init(bar_empty(ctl, s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_acc_full(ctl, a), 1);
@@ -437,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   ptx::tc_fence_before();
   __syncthreads();
   if constexpr (kCM > 1) {
-    // Peers multicast into this CTA's shared memory and signal its barriers:
-    // none may do so before every CTA of the cluster has initialised them.
+    // The pair's MMAs read both CTAs' shared memory and signal both CTAs'
+    // barriers: none may do so before every CTA has initialised them.
     ptx::cluster_arrive_relaxed();
     ptx::cluster_wait();
   }
@@ -468,7 +469,6 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   const int kb_end =
       (kPath == kPathSwap) ? (int)((int64_t)(split + 1) * p.num_k_blocks / p.splits) : p.num_k_blocks;
   const int crank = (kCM > 1) ? (int)(blockIdx.x % kCM) : 0;  // rank in the cluster
-  const uint16_t cmask = (uint16_t)((1u << kCM) - 1u);
   const int cluster_id = (int)(blockIdx.x / kCM);
   const int nclusters = (int)(gridDim.x / kCM);
 
@@ -614,25 +614,6 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
                     else
                       ptx::tma_load_2d(b_dst + (uint32_t)aa * 8192u, &p.ymap, full,
                                        nt * kBN + (crank * kBoxes + aa) * 64, k0);
-                  }
-                }
-              } else {
-                // This CTA's share of the Y tile, multicast to the whole cluster.
-                if constexpr (kYK) {
-                  constexpr int kRows = kBN / kCM;
-                  ptx::tma_load_2d_multicast(b_dst + (uint32_t)(crank * kRows) * 128u, &p.ymap, full, k0,
-                                             nt * kBN + crank * kRows, cmask);
-                } else if (p.y3d) {
-                  constexpr int kBoxes = kBN / 64 / kCM;
-                  ptx::tma_load_3d_multicast(b_dst + (uint32_t)(crank * kBoxes) * 8192u, &p.ymap, full, 0, k0,
-                                             nt * (kBN / 64) + crank * kBoxes, cmask);
-                } else {
-                  constexpr int kBoxes = kBN / 64 / kCM;
-#pragma unroll
-                  for (int aa = 0; aa < kBoxes; ++aa) {
-                    const int a = crank * kBoxes + aa;
-                    ptx::tma_load_2d_multicast(b_dst + (uint32_t)a * 8192u, &p.ymap, full, nt * kBN + a * 64, k0,
-                                               cmask);
                   }
                 }
               }
@@ -814,12 +795,10 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           if (issuer) {
             // the stores must have read the stage before it is released
             if (stored_stage) ptx::bulk_wait_read_all();
-            // frees the stage (in every cluster CTA: their producers multicast
-            // into it) once these MMAs finish
+            // frees the stage (a pair: in both CTAs, whose producers fill
+            // their halves of it) once these MMAs finish
             if constexpr (kPair)
               ptx::mma_commit_pair(bar_empty(ctl, stage), kPairMask);
-            else if constexpr (kCM > 1)
-              ptx::mma_commit_multicast(bar_empty(ctl, stage), cmask);
             else
               ptx::mma_commit(bar_empty(ctl, stage));
           }
@@ -1171,8 +1150,9 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   }
 
   if constexpr (kPath == kPathRows && kCM > 1) {
-    // Peers multicast into this CTA's shared memory and arrive on its
-    // barriers until their last MMA commits: leave only after all have drained.
+    // The pair leader's MMAs read this CTA's shared memory and its commits
+    // arrive on this CTA's barriers until the last one: leave only after both
+    // CTAs have drained.
     __syncwarp();
     ptx::cluster_sync_all();
   }
@@ -1226,14 +1206,9 @@ KernelFn select_kernel(const KernelKey& k) {
     if (k.pair) return nullptr;
     if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 1, false, 1);
     if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 1, false, 1);
-  } else if (k.cm == 2) {
-    if (k.pair) {
-      if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2, true, 1);
-      if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2, true, 1);
-    } else {
-      if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2, false, 1);
-      if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2, false, 1);
-    }
+  } else if (k.cm == 2 && k.pair) {
+    if (k.bn == 256) return AGMM_PICK(kPathRows, 256, 2, true, 1);
+    if (k.bn == 128) return AGMM_PICK(kPathRows, 128, 2, true, 1);
   }
   return nullptr;
 #undef AGMM_PICK

@@ -97,7 +97,7 @@ struct KernelKey {
   int bn;
   int cm;     // row path: CTAs per cluster along M (two: neighbouring row tiles)
   bool pair;  // cm == 2: one cta_group::2 MMA per pair, each CTA holding half the Y tile
-              // (otherwise each CTA multiplies alone and the Y tile is multicast)
+              // (a two-CTA cluster is always a pair; no copy is multicast)
   int atoms = 1;  // swap path: k blocks per pipeline stage (1 or 2)
 };
 

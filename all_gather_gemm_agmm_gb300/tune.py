@@ -73,13 +73,12 @@ def candidates(P: int, m: int, k: int, n: int, rt: bool, f16: bool = False, num_
         raw.append({"path": "swap", "dsmem_reduce": True, "tuned_table": False})
     # row tiles (for shapes that fit swapped tiles, only their main variants)
     tile_ns = [256, 128] if n % 256 == 0 else [128]
-    variants = itertools.product(tile_ns, (2, 1), (False, True), (True, False), (4, 8, 16))
+    # (a two-CTA cluster always multiplies as a CTA pair)
+    variants = itertools.product(tile_ns, (2, 1), (True, False), (4, 8, 16))
     if swap_ok:
-        variants = itertools.product(tile_ns, (2, 1), (False,), (True,), (8,))
-    for bn, cm, pair, sk, gm in variants:
-        if pair and cm != 2:
-            continue
-        raw.append({"path": "rows", "tile_n": bn, "cluster_m": cm, "cta_pair": pair, "stream_k": sk,
+        variants = itertools.product(tile_ns, (2, 1), (True,), (8,))
+    for bn, cm, sk, gm in variants:
+        raw.append({"path": "rows", "tile_n": bn, "cluster_m": cm, "cta_pair": cm == 2, "stream_k": sk,
                     "group_m": gm, "tuned_table": False})
     out, seen = [], set()
     for cfg in raw:

@@ -86,7 +86,8 @@ typedef struct {
   size_t smem_bytes; /* dynamic shared memory per CTA                            */
   int row_groups;    /* swapped tiles: groups of chunks, one MMA N each (else 1) */
   int cluster_m;     /* row tiles: CTAs per cluster sharing a Y tile (else 1)    */
-  int cta_pair;      /* row tiles: 1 when a cluster multiplies as a CTA pair     */
+  int cta_pair;      /* row tiles: 1 when a cluster multiplies as a CTA pair
+                        (always so for a two-CTA cluster)                       */
   int stream_k_tiles;/* row tiles: output tiles whose k blocks are shared        */
   int dsmem_reduce;  /* swapped tiles: 1 when k-split partials go through
                         distributed shared memory, 0 through device memory     */
@@ -115,10 +116,13 @@ typedef struct {
   int chunks;       /* 1: the ring's half-shard chunks; 2: whole-shard chunks */
   int box_rows;     /* X rows per TMA box: 8, 16, 32, 64 or 128               */
   int tile_n;       /* row tiles: MMA N, 128 or 256 (n must be a multiple)    */
-  int cluster_m;    /* row tiles: 1, or 2 neighbouring row tiles per cluster
-                       sharing each Y tile by TMA multicast                   */
-  int cta_pair;     /* row tiles: on = a 2-CTA cluster multiplies as one
-                       cta_group::2 pair (needs cluster_m 2)                  */
+  int cluster_m;    /* row tiles: 1, or 2 neighbouring row tiles per cluster,
+                       which multiply as one cta_group::2 pair, each CTA
+                       loading half of the shared Y tile                     */
+  int cta_pair;     /* row tiles: on = two-CTA clusters (needs cluster_m 2 or
+                       auto); off = one-CTA clusters (a two-CTA cluster is
+                       always a pair, so cluster_m 2 with cta_pair off is
+                       AGMM_ERR_UNSUPPORTED)                                  */
   int stages;       /* pipeline stages, 2..8: an upper bound that shared
                        memory may lower (a swapped k-split reduction that
                        receives in shared memory may raise it)                */
@@ -161,7 +165,8 @@ agmm_status_t agmm_plan(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_
  * agmm_plan.  Returns AGMM_ERR_INVALID_ARG for a field outside its range, and
  * AGMM_ERR_UNSUPPORTED when a set field cannot hold for this shape (swapped
  * tiles for more than 256 padded rows, tile_n not dividing n, a CTA pair
- * without a 2-CTA cluster, an empty row group, a box height whose swapped
+ * without a 2-CTA cluster or a 2-CTA cluster without the pair, an empty row
+ * group, a box height whose swapped
  * rows exceed 256).
  */
 agmm_status_t agmm_plan_config(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_dtype_t dtype,

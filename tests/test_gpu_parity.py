@@ -149,23 +149,25 @@ def test_stream_k_split(agmm, streamk, monkeypatch):
 @pytest.mark.parametrize("case", [(3, 200, 1024, 512, False), (5, 300, 512, 256, True), (8, 130, 256, 640, True),
                                   (4, 256, 768, 768, False)])
 def test_cluster_variants(agmm, case, monkeypatch):
-    # Row tiles in clusters of two: either one cta_group::2 MMA per pair (each
-    # CTA holds half the Y tile) or one MMA per CTA with the Y tile multicast.
-    # Without stream-K the multicast variant is bitwise equal to one CTA per
-    # cluster; every variant meets the oracle tolerance.  Odd row-tile counts
-    # exercise an idle second CTA.
+    # Row tiles either one CTA per cluster, or clusters of two that multiply
+    # as one cta_group::2 MMA per pair (each CTA loads and holds half the Y
+    # tile; no copy is multicast).  Both meet the oracle tolerance; odd
+    # row-tile counts exercise an idle second CTA.  A two-CTA cluster without
+    # the pair is not a plan.
     P, m, k, n, rt = case
     xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=6)
     ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
     monkeypatch.setenv("AGMM_STREAMK", "0")
-    outs = {}
-    for name, cm, pair in (("single", "1", "0"), ("multicast", "2", "0"), ("pair", "2", "1")):
+    for name, cm, pair in (("single", "1", "0"), ("pair", "2", "1")):
         monkeypatch.setenv("AGMM_CM", cm)
         monkeypatch.setenv("AGMM_PAIR", pair)
         o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=P - 1)
-        check(o, ref32, f"{name} {plan.info()}")
-        outs[name] = o
-    assert torch.equal(outs["single"].view(torch.int16), outs["multicast"].view(torch.int16))
+        info = plan.info()
+        assert info["cluster_m"] == int(cm) and info["cta_pair"] == int(pair == "1"), info
+        check(o, ref32, f"{name} {info}")
+    with pytest.raises(agmm.AgmmError) as err:
+        agmm.Plan(P, m, k, n, rt, config={"path": "rows", "cluster_m": 2, "cta_pair": False})
+    assert err.value.status == agmm.AGMM_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("mode", ["half", "whole"])

@@ -81,8 +81,12 @@ def test_infeasible_set_fields_are_unsupported():
     assert status_of(8, 64, 512, 256, path="swap") == agmm.AGMM_ERR_UNSUPPORTED
     # tile_n must divide n
     assert status_of(8, 1000, 512, 384, path="rows", tile_n=256) == agmm.AGMM_ERR_UNSUPPORTED
-    # a CTA pair needs a 2-CTA cluster
+    # a CTA pair needs a 2-CTA cluster, and a 2-CTA cluster is always a pair
+    # (no copy is multicast to a cluster)
     assert status_of(8, 1000, 512, 512, cluster_m=1, cta_pair=True) == agmm.AGMM_ERR_UNSUPPORTED
+    assert status_of(8, 1000, 512, 512, cluster_m=2, cta_pair=False) == agmm.AGMM_ERR_UNSUPPORTED
+    # cta_pair off alone means one-CTA clusters
+    assert pv(8, 1000, 512, 512, cta_pair=False)["cluster_m"] == 1
     # 2 chunks cannot make 4 non-empty row groups
     assert status_of(2, 16, 256, 256, chunks="whole", box_rows=16, row_groups=4) == agmm.AGMM_ERR_UNSUPPORTED
 
@@ -210,7 +214,7 @@ def test_random_configs_plan_or_fail_cleanly():
         assert info["box_rows"] in (8, 16, 32, 64, 128), (cfg, info)
         if info["path"] == 0:
             assert info["tile_n"] in (128, 256) and n % info["tile_n"] == 0, (cfg, info)
-            assert info["cta_pair"] in (0, 1) and (info["cta_pair"] == 0 or info["cluster_m"] == 2), (cfg, info)
+            assert info["cta_pair"] in (0, 1) and info["cta_pair"] == int(info["cluster_m"] == 2), (cfg, info)
         else:
             assert info["tile_n"] <= 256 and 1 <= info["splits"] <= 16, (cfg, info)
     assert planned > 200
