@@ -687,8 +687,10 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   return AGMM_OK;
 }
 
+// ws_bytes: the workspace bytes the call uses (agmm_workspace_bytes); the
+// workspace must not overlap O, Y or a shard.
 agmm_status_t check_run_args(agmm_plan_s* pl, const void* const* xs, const void* y, void* o, int my_id,
-                             void* ws) {
+                             void* ws, size_t ws_bytes) {
   if (!pl) return fail(AGMM_ERR_INVALID_ARG, "plan is NULL");
   if (!xs || !y || !o || !ws) return fail(AGMM_ERR_INVALID_ARG, "a pointer argument is NULL");
   if (my_id < 0 || my_id >= pl->P) return fail(AGMM_ERR_INVALID_ARG, "my_id must be in [0, P)");
@@ -699,10 +701,14 @@ agmm_status_t check_run_args(agmm_plan_s* pl, const void* const* xs, const void*
     if (!xs[r]) return fail(AGMM_ERR_INVALID_ARG, "shard pointer " + std::to_string(r) + " is NULL");
     if (!aligned16(xs[r])) return fail(AGMM_ERR_ALIGNMENT, "shard " + std::to_string(r) + " is not 16-byte aligned");
     if (overlaps(xs[r], xbytes, o, obytes)) return fail(AGMM_ERR_INVALID_ARG, "O overlaps a shard");
+    if (overlaps(xs[r], xbytes, ws, ws_bytes))
+      return fail(AGMM_ERR_INVALID_ARG, "the workspace overlaps shard " + std::to_string(r));
   }
   if (!aligned16(y) || !aligned16(o) || !aligned16(ws))
     return fail(AGMM_ERR_ALIGNMENT, "Y, O and the workspace must be 16-byte aligned");
   if (overlaps(y, ybytes, o, obytes)) return fail(AGMM_ERR_INVALID_ARG, "O overlaps Y");
+  if (overlaps(y, ybytes, ws, ws_bytes)) return fail(AGMM_ERR_INVALID_ARG, "the workspace overlaps Y");
+  if (overlaps(o, obytes, ws, ws_bytes)) return fail(AGMM_ERR_INVALID_ARG, "the workspace overlaps O");
   return AGMM_OK;
 }
 
@@ -804,7 +810,7 @@ agmm_status_t run_unfused_on_scratch(agmm_plan_s* plan, const void* const* x_sha
     return fail(AGMM_ERR_INVALID_ARG, "this problem needs " + std::to_string(need) +
                                           " bytes of scratch but the static scratch holds " +
                                           std::to_string(scratch_bytes) + "; use agmm_run_unfused");
-  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, scratch);
+  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, scratch, need);
   if (st != AGMM_OK) return st;
   uint8_t* base = static_cast<uint8_t*>(scratch);
   agmm_plan_s* gemm = plan->P == 1 ? plan : plan->sub;
@@ -865,7 +871,7 @@ size_t agmm_workspace_bytes(agmm_plan_t plan, int unfused) {
 
 agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o, int my_id,
                        void* workspace, void* stream) {
-  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace);
+  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace, agmm_workspace_bytes(plan, 0));
   if (st != AGMM_OK) return st;
   return launch_fused(plan, x_shards, y, o, my_id, workspace, static_cast<uint8_t*>(workspace) + kStatusBytes,
                       static_cast<cudaStream_t>(stream));
@@ -873,7 +879,7 @@ agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void
 
 agmm_status_t agmm_run_gather(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o, void* xcat,
                               int my_id, void* workspace, void* stream) {
-  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace);
+  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace, agmm_workspace_bytes(plan, 0));
   if (st != AGMM_OK) return st;
   if (!xcat) return fail(AGMM_ERR_INVALID_ARG, "xcat is NULL");
   if (!aligned16(xcat)) return fail(AGMM_ERR_ALIGNMENT, "xcat must be 16-byte aligned");
@@ -895,7 +901,7 @@ agmm_status_t agmm_run_gather(agmm_plan_t plan, const void* const* x_shards, con
 
 agmm_status_t agmm_run_unfused(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o,
                                int my_id, void* workspace, void* stream) {
-  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace);
+  agmm_status_t st = check_run_args(plan, x_shards, y, o, my_id, workspace, agmm_workspace_bytes(plan, 1));
   if (st != AGMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (plan->P == 1)
@@ -924,7 +930,8 @@ agmm_status_t agmm_run_host(agmm_plan_t plan, const void* const* x_host, const v
     return fail(AGMM_ERR_INVALID_ARG, "a pointer argument is NULL");
   for (int r = 0; r < plan->P; ++r)
     if (!x_host[r] || !x_dev[r]) return fail(AGMM_ERR_INVALID_ARG, "a shard pointer is NULL");
-  agmm_status_t st = check_run_args(plan, const_cast<const void* const*>(x_dev), y_dev, o_dev, my_id, workspace);
+  agmm_status_t st = check_run_args(plan, const_cast<const void* const*>(x_dev), y_dev, o_dev, my_id, workspace,
+                                    agmm_workspace_bytes(plan, 0));
   if (st != AGMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t xbytes = (size_t)plan->m_pd * plan->k * 2;

@@ -1,14 +1,15 @@
 // agmm_noalloc.cu -- an allocation-free variant of the unfused path.
 //
 // Some callers cannot allocate device memory at the point where they run the
-// all-gather matmul: code that runs while a CUDA graph is being captured
-// (cudaMalloc is not allowed inside a capture), code under an allocator that
-// owns all device memory and forbids outside allocations, and latency-critical
-// loops where cudaMalloc's implicit device synchronisation is unacceptable.
-// agmm_run_unfused_noalloc serves them: its scratch (status words, the
-// gathered [P*m_per_device, k] buffer and the split-tail counters and
-// partials) lives in one file-scope device array of AGMM_STATIC_SCRATCH_BYTES,
-// which every GPU that loads this library holds until the process exits.
+// all-gather matmul: code under a framework allocator that has reserved the
+// device's memory for itself (an outside cudaMalloc can fail or fragment that
+// pool), and latency-critical loops where cudaMalloc's and cudaFree's
+// implicit device synchronisation is unacceptable.  agmm_run_unfused_noalloc
+// serves them: its scratch (status words, the gathered [P*m_per_device, k]
+// buffer and the split-tail counters and partials) lives in one file-scope
+// device array of AGMM_STATIC_SCRATCH_BYTES, which every GPU that loads this
+// library holds until the process exits.  The array's device address is
+// looked up once per device and kept; a device reset invalidates it.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -5,12 +5,19 @@
                     [--impl ours|reference] [--sweep]
 
 One step is one fused all-gather matmul (agmm_run) over one batch of synthetic
-inputs resident in device memory.  Timing: W untimed warm-up steps, then
-exactly K steps bracketed by a barrier and a device synchronize, on CUDA
-events recorded on the stream the kernels are launched on.  Between timed
-steps the inputs and outputs rotate over R replicas whose total footprint
-exceeds three times the L2 size, so no step reads data a previous step left
-in L2.  Rank 0 prints one JSON line.
+inputs resident in device memory; the default workload is the prefill-like
+P=8, m_per_device=2048, k=8192, n=7168 problem with Y stored [n, k].
+
+Timing: W untimed warm-up steps, then batches of exactly K steps.  Each batch
+is one replay of a CUDA graph that holds exactly K steps, step i on replica
+i mod R, so the inputs and outputs rotate over R replicas (footprint above
+three times the L2 size: no step reads data a previous step left in L2)
+whatever K is.  Each batch is bracketed by a barrier and a device synchronize
+and timed with CUDA events on the stream the kernels are launched on; the
+line reports the median batch (at least 7 batches, and at least a second of
+timed work for the headline).  The unfused and gathered-LHS paths, and the
+sub-results of the decode-like and mid-size workloads, are timed the same
+way.  Rank 0 prints one JSON line.
 
 With N > 1 (torchrun) every rank runs an independent replica of the
 workload on its own GPU ("replicas only": the method's exchange is between
@@ -33,7 +40,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused all-gather-GEMM TFLOP/s and % of roofline (tensor peak / HBM GB/s) on 1 GB300"
-DEFAULT_WORKLOAD = "c2_decode"
+DEFAULT_WORKLOAD = "c4_prefill"
 L2_BYTES_FALLBACK = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -218,9 +225,10 @@ def build_replicas(w, R, device, seed=1234, dtype="bf16"):
     return reps
 
 
-def time_graph(step_fns, K, warmup, stream):
-    """Capture one round of R steps (one per replica) in a CUDA graph, run W
-    warm-up steps, then time exactly K steps with events on `stream`."""
+def capture_steps(step_fns, K, warmup, stream):
+    """A CUDA graph of exactly K steps: step i runs on replica i mod R, so the
+    replicas rotate inside the graph whatever K is.  W warm-up steps run
+    eagerly first, then one untimed replay."""
     import torch
 
     R = len(step_fns)
@@ -229,37 +237,72 @@ def time_graph(step_fns, K, warmup, stream):
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        for fn in step_fns:
-            fn(stream.cuda_stream)
+        for i in range(K):
+            step_fns[i % R](stream.cuda_stream)
     with torch.cuda.stream(stream):
         graph.replay()
     torch.cuda.synchronize()
     return graph
 
 
-def run_timed(graph, step_fns, K, stream, sampler=None):
+def time_batches(graph, stream, batches, sampler=None):
+    """Seconds of each of `batches` replays of a K-step graph, each bracketed
+    by a barrier and a device synchronize, timed with events on `stream`."""
+    import torch
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    times = []
+    if sampler:
+        sampler.start()
+    for _ in range(batches):
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            graph.replay()
+            end.record(stream)
+        end.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        times.append(start.elapsed_time(end) / 1000.0)
+    clocks = sampler.stop() if sampler else None
+    return times, clocks
+
+
+def estimate_step_s(step_fns, stream, n=None):
+    """Rough seconds per step from a few eager launches (sizes K and batches)."""
     import torch
 
     R = len(step_fns)
-    full, rest = divmod(K, R)
+    n = n or max(3, min(2 * R, 50))
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    barrier()
     torch.cuda.synchronize()
-    if sampler:
-        sampler.start()
     with torch.cuda.stream(stream):
         start.record(stream)
-        for _ in range(full):
-            graph.replay()
-        for i in range(rest):
-            step_fns[i](stream.cuda_stream)
+        for i in range(n):
+            step_fns[i % R](stream.cuda_stream)
         end.record(stream)
     end.synchronize()
-    torch.cuda.synchronize()
-    barrier()
-    clocks = sampler.stop() if sampler else None
-    return start.elapsed_time(end) / 1000.0, clocks
+    return max(start.elapsed_time(end) / 1000.0 / n, 1e-7)
+
+
+def measure(step_fns, K, warmup, stream, device, min_batches=7, min_timed_s=0.5, max_batches=400,
+            sampler=None):
+    """Median over batches of the seconds per step, K steps per batch; the
+    max over ranks of each rank's median."""
+    import statistics as st
+
+    est = estimate_step_s(step_fns, stream)
+    graph = capture_steps(step_fns, K, warmup, stream)
+    B = int(min(max_batches, max(min_batches, -(-min_timed_s // max(est * K, 1e-7)))))
+    times, clocks = time_batches(graph, stream, B, sampler)
+    del graph
+    med = st.median(times)
+    med = reduce_max(med, device)
+    return {"s_per_step": med / K, "K": K, "batches": B, "batch_ms_min": min(times) * 1e3,
+            "batch_ms_max": max(times) * 1e3}, clocks
 
 
 def cpu_oracle_sample(w, target_s=8.0, dtype="bf16"):
@@ -292,6 +335,114 @@ def cpu_oracle_sample(w, target_s=8.0, dtype="bf16"):
                       f"in {calls} calls, {spent:.1f} s", "seconds": spent}
 
 
+def roofline_of(w, s_per_step, peaks, peak_src):
+    """Roofline of one fused launch: algorithmic FLOPs (2*M*k*n) or unique
+    bytes (2*(M*k + k*n + M*n)) over the measured seconds per launch, against
+    the measured peak that bounds the shape."""
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ai = w.flops / w.unique_bytes
+    if ai < ridge:
+        achieved = w.unique_bytes / s_per_step / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = w.flops / s_per_step / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])}
+    roof["traffic"] = recorded_traffic(w.name)
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["kernel"] = "agmm_fused_sm103a"
+    roof["algorithmic_bytes_per_launch"] = w.unique_bytes
+    roof["flops_per_launch"] = w.flops
+    roof["roofline_time_us"] = max(w.flops / (peaks["bf16_tflops"] * 1e12),
+                                   w.unique_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+    roof["frac_of_roofline_time"] = roof["roofline_time_us"] / (s_per_step * 1e6)
+    return roof
+
+
+class WorkloadBench:
+    """Replicas of one workload in device memory (footprint > 3x L2), a plan,
+    and the step functions of the fused, unfused and gathered-LHS paths."""
+
+    def __init__(self, w, device, dtype="bf16"):
+        import torch
+
+        import all_gather_gemm_agmm_gb300 as agmm
+
+        self.w = w
+        self.device = device
+        self.l2 = torch.cuda.get_device_properties(device).L2_cache_size or L2_BYTES_FALLBACK
+        self.R = max(2, -(-3 * self.l2 // w.unique_bytes))
+        self.reps = build_replicas(w, self.R, device, dtype=dtype)
+        self.plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, f16=dtype == "f16")
+        self.ws = self.plan.new_workspace(False, device=device)
+        self.ws_unf = self.plan.new_workspace(True, device=device)
+        # inputs and zeroed workspaces come from the current stream; the
+        # kernels run on another stream
+        torch.cuda.synchronize()
+
+    def fused(self):
+        plan, ws, my_id = self.plan, self.ws, self.w.my_id
+
+        def step(rep):
+            xp = [x.data_ptr() for x in rep[0]]
+            yp, op, wp = rep[1].data_ptr(), rep[2].data_ptr(), ws.data_ptr()
+            return lambda s: plan.run_ptrs(xp, yp, op, my_id, wp, s)
+
+        return [step(r) for r in self.reps]
+
+    def unfused(self):
+        plan, ws, my_id = self.plan, self.ws_unf, self.w.my_id
+        return [(lambda rep: (lambda s: plan.run_unfused(rep[0], rep[1], rep[2], my_id, ws, s)))(r)
+                for r in self.reps]
+
+    def gathered(self):
+        import torch
+
+        plan, ws, my_id = self.plan, self.ws, self.w.my_id
+        self.xcats = [torch.empty((self.w.M, self.w.k), dtype=r[2].dtype, device=self.device) for r in self.reps]
+        torch.cuda.synchronize()
+        return [(lambda rep, xc: (lambda s: plan.run_gather(rep[0], rep[1], rep[2], xc, my_id, ws, s)))(r, xc)
+                for r, xc in zip(self.reps, self.xcats)]
+
+
+def sub_result(args, name, device, stream, peaks, peak_src):
+    """Fused, unfused and gathered-LHS timings of another workload, measured
+    the same way as the headline (K-step graphs, median of batches); K is
+    chosen so that a batch lasts at least about 2 ms."""
+    import torch
+
+    from all_gather_gemm_agmm_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS[name]
+    wb = WorkloadBench(w, device, args.dtype)
+    fused = wb.fused()
+    est = estimate_step_s(fused, stream)
+    K = int(max(args.steps or 20, min(2000, -(-2e-3 // est))))
+    f, _ = measure(fused, K, args.warmup, stream, device)
+    wb.plan.query_status(wb.ws, stream)
+    u, _ = measure(wb.unfused(), K, args.warmup, stream, device)
+    wb.plan.query_status(wb.ws_unf, stream)
+    g, _ = measure(wb.gathered(), K, args.warmup, stream, device)
+    wb.plan.query_status(wb.ws, stream)
+    roof = roofline_of(w, f["s_per_step"], peaks, peak_src)
+    out = {"value": w.flops / f["s_per_step"] / 1e12 * dist_env()[0], "unit": "TFLOP/s",
+           "ms_per_step": f["s_per_step"] * 1e3, "steps": K, "batches": f["batches"],
+           "config": {"P": w.P, "m_per_device": w.m_per_device, "k": w.k, "n": w.n,
+                      "rhs_transpose": w.rhs_transpose, "my_id": w.my_id, "replicas": wb.R,
+                      "plan": wb.plan.info()},
+           "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic",
+                                             "roofline_time_us")},
+           "unfused_ms_per_step": u["s_per_step"] * 1e3, "fused_speedup": u["s_per_step"] / f["s_per_step"],
+           "with_gathered_ms_per_step": g["s_per_step"] * 1e3,
+           "with_gathered_vs_unfused": u["s_per_step"] / g["s_per_step"]}
+    del wb
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_ours(args, w):
     import torch
 
@@ -301,62 +452,30 @@ def bench_ours(args, w):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     init_dist("nccl")
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size or L2_BYTES_FALLBACK
-    per_rep = w.unique_bytes
-    R = max(2, -(-3 * l2 // per_rep))
-    reps = build_replicas(w, R, device, dtype=args.dtype)
-    plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, f16=args.dtype == "f16")
-    info = plan.info()
-    ws = plan.new_workspace(False, device=device)
-    ws_unf = plan.new_workspace(True, device=device)
+    peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device=device)
-    # inputs and zeroed workspaces come from the current stream; the kernels
-    # run on `stream`
-    torch.cuda.synchronize()
+    wb = WorkloadBench(w, device, args.dtype)
+    plan, ws = wb.plan, wb.ws
+    info = plan.info()
+    K = args.steps
 
-    def fused_step(rep):
-        xs, y, o = rep
-        xp = [x.data_ptr() for x in xs]
-        return lambda s: plan.run_ptrs(xp, y.data_ptr(), o.data_ptr(), w.my_id, ws.data_ptr(), s)
-
-    def unfused_step(rep):
-        xs, y, o = rep
-        return lambda s: plan.run_unfused(xs, y, o, w.my_id, ws_unf, s)
-
-    fused = [fused_step(r) for r in reps]
-    graph = time_graph(fused, args.steps, args.warmup, stream)
-    # estimate step time, then pick K when not given
-    est, _ = run_timed(graph, fused, R, stream)
-    K = args.steps if args.steps else int(max(R, min(500000, round(1.5 / max(est / R, 1e-7)))))
+    # the headline: the fused path, K-step graphs, median of batches, clocks
+    # sampled during the timed batches
     sampler = ClockSampler(gpu_uuid(device))
-    elapsed, clocks = run_timed(graph, fused, K, stream, sampler)
+    fz, clocks = measure(wb.fused(), K, args.warmup, stream, device, min_timed_s=1.0, sampler=sampler)
     plan.query_status(ws, stream)
-    value, tmax = aggregate_throughput(w.flops * K / 1e12, elapsed, device)
-    ms_per_step = tmax / K * 1e3
+    s_step = fz["s_per_step"]
+    value = w.flops / s_step / 1e12 * ws_n  # every rank runs the same work
+    ms_per_step = s_step * 1e3
 
-    # unfused comparison (same replicas, same method)
-    unf = [unfused_step(r) for r in reps]
-    g2 = time_graph(unf, K, args.warmup, stream)
-    K2 = max(R, min(K, int(round(1.0 / max(est / R, 1e-7)))))
-    el2, _ = run_timed(g2, unf, K2, stream)
-    plan.query_status(ws_unf, stream)
-    unf_ms = reduce_max(el2, device) / K2 * 1e3
-    del g2
-
-    # the fused path that also writes the gathered LHS (what the unfused path
-    # materialises too): one gathered buffer per replica, same method (a
-    # CTA-pair plan runs it through its companion plan without the pair)
-    gath_ms = None
-    if True:
-        xcats = [torch.empty((w.M, w.k), dtype=r[2].dtype, device=device) for r in reps]
-        torch.cuda.synchronize()
-        gath = [(lambda rep, xc: (lambda s: plan.run_gather(rep[0], rep[1], rep[2], xc, w.my_id, ws, s)))(r, xc)
-                for r, xc in zip(reps, xcats)]
-        g3 = time_graph(gath, K, args.warmup, stream)
-        el3, _ = run_timed(g3, gath, K2, stream)
-        plan.query_status(ws, stream)
-        gath_ms = reduce_max(el3, device) / K2 * 1e3
-        del g3, xcats
+    # unfused comparison and the fused path that also writes the gathered LHS
+    # (what the unfused path materialises too): same replicas, same method
+    uf, _ = measure(wb.unfused(), K, args.warmup, stream, device)
+    plan.query_status(wb.ws_unf, stream)
+    gz, _ = measure(wb.gathered(), K, args.warmup, stream, device)
+    plan.query_status(ws, stream)
+    unf_ms, gath_ms = uf["s_per_step"] * 1e3, gz["s_per_step"] * 1e3
+    del wb.xcats
 
     # end to end through the C ABI from pinned host memory.  Two steps are in
     # flight: each slot has its own device buffers, plan, workspace and
@@ -364,6 +483,7 @@ def bench_ours(args, w):
     # download.  Every step still uploads all of its inputs and reads its O.
     e2e = None
     if not args.no_e2e:
+        reps = wb.reps
         xs_h = [x.cpu().pin_memory() for x in reps[0][0]]
         y_h = reps[0][1].cpu().pin_memory()
         slots = []
@@ -404,46 +524,40 @@ def bench_ours(args, w):
         e2e = {"value": e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * (w.M * w.k + w.k * w.n),
                "d2h_bytes_per_step": 2 * w.M * w.n, "steps": Ke, "ms_per_step": e_el / Ke * 1e3,
                "pipelining": "2 steps in flight (two device buffer sets, two streams)"}
+        del slots, xs_h, y_h
+    R, per_rep, l2 = wb.R, w.unique_bytes, wb.l2
+    del wb
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
-    peaks, peak_src = load_peaks()
-    launch_s = tmax / K
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    ai = w.flops / w.unique_bytes
-    if ai < ridge:
-        achieved = w.unique_bytes / launch_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"]}
-    else:
-        achieved = w.flops / launch_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"],
-                "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])}
-    roof["traffic"] = recorded_traffic(w.name)
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
-    roof["kernel"] = "agmm_fused_sm103a"
-    roof["algorithmic_bytes_per_launch"] = w.unique_bytes
-    roof["flops_per_launch"] = w.flops
-    roof["roofline_time_us"] = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.unique_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
-    roof["frac_of_roofline_time"] = roof["roofline_time_us"] / (launch_s * 1e6)
+    subs = {}
+    if not args.no_sub:
+        for name in [n for n in args.sub.split(",") if n and n != w.name]:
+            subs[name] = sub_result(args, name, device, stream, peaks, peak_src)
 
+    roof = roofline_of(w, s_step, peaks, peak_src)
     result = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_n, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": args.dtype, "data": "synthetic (seeded torch.Generator on device; shapes of the workload)",
         "config": {"workload": w.name, "P": w.P, "m_per_device": w.m_per_device, "k": w.k, "n": w.n,
                    "rhs_transpose": w.rhs_transpose, "my_id": w.my_id, "dist": w.dist,
-                   "l2": f"{R} rotating input/output replicas, {R * per_rep / 2**20:.0f} MiB > 3x L2 "
-                         f"({l2 / 2**20:.0f} MiB)",
-                   "timing": "CUDA graph of one replica round, events on the launch stream",
+                   "l2": f"inputs larger than L2: {R} rotating input/output replicas, "
+                         f"{R * per_rep / 2**20:.0f} MiB > 3x L2 ({l2 / 2**20:.0f} MiB)",
+                   "timing": f"median of {fz['batches']} batches, each one replay of a CUDA graph of exactly "
+                             f"{K} steps (step i on replica i mod {R}), events on the launch stream, "
+                             "barrier and synchronize around each batch; max over ranks",
+                   "batch_ms_range": [fz["batch_ms_min"], fz["batch_ms_max"]],
                    "parallelism": f"replicas x{ws_n}", "plan": info},
         "roofline": roof,
-        "unfused": {"ms_per_step": unf_ms, "value": w.flops / (unf_ms / 1e3) / 1e12 * ws_n, "steps": K2,
-                    "fused_speedup": unf_ms / ms_per_step},
-        "with_gathered": None if gath_ms is None else {
-            "ms_per_step": gath_ms, "steps": K2, "vs_unfused": unf_ms / gath_ms,
-            "cost_over_fused": gath_ms / ms_per_step},
+        "unfused": {"ms_per_step": unf_ms, "value": w.flops / (unf_ms / 1e3) / 1e12 * ws_n, "steps": K,
+                    "batches": uf["batches"], "fused_speedup": unf_ms / ms_per_step},
+        "with_gathered": {"ms_per_step": gath_ms, "steps": K, "batches": gz["batches"],
+                          "vs_unfused": unf_ms / gath_ms, "cost_over_fused": gath_ms / ms_per_step},
+        "sub_results": subs,
         "e2e": e2e,
         "gpu_launches": K,
+        "gpu_launches_note": "fused kernel launches per timed batch (one per step)",
         "clocks": clocks,
     }
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
@@ -453,41 +567,38 @@ def bench_ours(args, w):
 
 
 def bench_sweep(args):
-    """Fused vs unfused device time at every point of the k=5120, n=2560 sweep."""
+    """Fused vs unfused device time at every point of the k=5120, n=2560
+    sweep, each timed like the headline (K-step graphs, median of batches)."""
     import torch
 
-    import all_gather_gemm_agmm_gb300 as agmm
     from all_gather_gemm_agmm_gb300.inputs import SWEEP
 
     torch.cuda.set_device(0)
     device = torch.device("cuda", 0)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size or L2_BYTES_FALLBACK
-    peaks, _ = load_peaks()
+    peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device=device)
+    names = set(args.sweep_points.split(",")) if args.sweep_points else None
     for w in SWEEP:
-        R = max(2, -(-3 * l2 // w.unique_bytes))
-        reps = build_replicas(w, R, device, dtype=args.dtype)
-        plan = agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, f16=args.dtype == "f16")
-        ws = plan.new_workspace(False, device=device)
-        wsu = plan.new_workspace(True, device=device)
-        torch.cuda.synchronize()  # zeroed workspaces and inputs before launches on `stream`
-        fused = [(lambda rep: (lambda s: plan.run(rep[0], rep[1], rep[2], w.my_id, ws, s)))(r) for r in reps]
-        unf = [(lambda rep: (lambda s: plan.run_unfused(rep[0], rep[1], rep[2], w.my_id, wsu, s)))(r) for r in reps]
-        g1 = time_graph(fused, 0, 3, stream)
-        est, _ = run_timed(g1, fused, R, stream)
-        K = int(max(R, min(100000, round(0.3 / max(est / R, 1e-7)))))
-        t1, _ = run_timed(g1, fused, K, stream)
-        g2 = time_graph(unf, 0, 3, stream)
-        t2, _ = run_timed(g2, unf, K, stream)
-        plan.query_status(ws, stream)
-        f_us, u_us = t1 / K * 1e6, t2 / K * 1e6
-        roof_us = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.unique_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+        if names and w.name not in names:
+            continue
+        wb = WorkloadBench(w, device, args.dtype)
+        fused = wb.fused()
+        est = estimate_step_s(fused, stream)
+        K = int(max(args.steps or 20, min(2000, -(-2e-3 // est))))
+        f, _ = measure(fused, K, args.warmup, stream, device)
+        wb.plan.query_status(wb.ws, stream)
+        u, _ = measure(wb.unfused(), K, args.warmup, stream, device)
+        wb.plan.query_status(wb.ws_unf, stream)
+        f_us, u_us = f["s_per_step"] * 1e6, u["s_per_step"] * 1e6
+        roof = roofline_of(w, f["s_per_step"], peaks, peak_src)
         print(json.dumps({"sweep_point": w.name, "P": w.P, "m_per_device": w.m_per_device,
                           "rhs_transpose": w.rhs_transpose, "fused_us": f_us, "unfused_us": u_us,
-                          "fused_tflops": w.flops / (f_us * 1e-6) / 1e12, "roofline_us": roof_us,
-                          "frac_of_roofline": roof_us / f_us, "fused_faster": f_us < u_us,
-                          "plan": plan.info()}), flush=True)
-        del g1, g2, reps
+                          "fused_tflops": w.flops / (f_us * 1e-6) / 1e12, "roofline_us": roof["roofline_time_us"],
+                          "bound": roof["bound"], "frac": roof["frac"],
+                          "frac_of_roofline": roof["frac_of_roofline_time"], "fused_faster": f_us < u_us,
+                          "steps": K, "batches": f["batches"], "plan": wb.plan.info()}), flush=True)
+        del wb, fused
+        torch.cuda.synchronize()
         torch.cuda.empty_cache()
 
 
@@ -535,12 +646,16 @@ def bench_reference(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 1.5 s worth)")
+    ap.add_argument("--steps", type=int, default=20, help="steps per timed batch (one K-step CUDA graph)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true", help="fused vs unfused at every sweep point")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="skip the other workloads' sub-results")
+    ap.add_argument("--sub", default="c2_decode,c3_mid",
+                    help="comma-separated workloads measured as sub-results of the same line")
+    ap.add_argument("--sweep-points", default="", help="with --sweep: comma-separated sweep point names")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="element type of X, Y and O (fp16: the tutorial's float16 variant)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -549,6 +664,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
     from all_gather_gemm_agmm_gb300.inputs import WORKLOADS
 
     w = WORKLOADS[args.workload]

@@ -181,6 +181,9 @@ void agmm_destroy(agmm_plan_t plan);
  * the unfused path adds the gathered [P*m_per_device, k] buffer (input type) at
  * offset 256.  The workspace must be zero-filled before its first use and
  * must not be shared by runs that overlap on the device.  Returns 0 for NULL.
+ * After agmm_query_status has reported AGMM_ERR_TIMEOUT, zero-fill the whole
+ * workspace again before its next use: a run that gave up may leave split
+ * counters behind it.
  */
 size_t agmm_workspace_bytes(agmm_plan_t plan, int unfused);
 
@@ -191,7 +194,8 @@ size_t agmm_workspace_bytes(agmm_plan_t plan, int unfused);
  *   y         device pointer, [k, n] or (rhs_transpose) [n, k]
  *   o         device pointer, [P*m_per_device, n]; must not overlap an input
  *   my_id     this rank's index in [0, P): ring step 0 starts at shard my_id
- *   workspace device pointer to agmm_workspace_bytes(plan, 0) bytes
+ *   workspace device pointer to agmm_workspace_bytes(plan, 0) bytes; must
+ *             not overlap O, Y or a shard
  *   stream    a cudaStream_t (NULL: the legacy default stream)
  *
  * Every device pointer must be 16-byte aligned (TMA: global addresses and
@@ -238,23 +242,28 @@ agmm_status_t agmm_run_unfused(agmm_plan_t plan, const void* const* x_shards, co
 
 /*
  * agmm_run_unfused_noalloc -- agmm_run_unfused without a caller workspace and
- * without allocating: for callers that cannot allocate device memory where
- * they run this (inside CUDA graph capture, under an allocator that owns all
- * device memory, or in latency-critical loops that cannot afford cudaMalloc's
- * implicit synchronisation).  The pages have no counterpart; this is a
- * convenience of this library.
+ * without allocating device memory.  The pages have no counterpart; this is a
+ * convenience of this library for callers that cannot allocate at the point
+ * where they run the product: code under a framework allocator that has
+ * reserved the device's memory for itself (a cudaMalloc of its own there can
+ * fail or fragment that pool), and latency-critical loops that cannot afford
+ * cudaMalloc's and cudaFree's implicit device synchronisation.
  *
- * The scratch is one file-scope device array of AGMM_STATIC_SCRATCH_BYTES that
- * every GPU loading this library holds until the process exits.  A problem
- * whose agmm_workspace_bytes(plan, 1) exceeds it is rejected with
- * AGMM_ERR_INVALID_ARG (nothing is launched).  The first call on a device looks
- * up the array's device address (cudaGetSymbolAddress); make that first call
- * before any stream capture.  Each call clears the scratch's status words and
- * counters on `stream`, then gathers and multiplies.  All calls share the one
- * array: calls that overlap on the device (different streams without ordering)
- * race and corrupt each other.  Device-side wait timeouts of these calls are
- * recorded in the shared scratch and are not reported to the caller.
- * Arguments, alignment rules and result are those of agmm_run.
+ * The scratch is one file-scope device array of AGMM_STATIC_SCRATCH_BYTES (64
+ * MiB) that every GPU loading this library holds until the process exits.  A
+ * problem whose agmm_workspace_bytes(plan, 1) exceeds it is rejected with
+ * AGMM_ERR_INVALID_ARG (nothing is launched).  The first call on a device,
+ * with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress) and keeps it for later calls on that device: make
+ * that first call before any stream capture, and note that a device reset
+ * (cudaDeviceReset) invalidates the kept address, so no call may follow a
+ * reset in the same process.  Each call clears the scratch's status words and
+ * counters on `stream`, then gathers and multiplies; no call allocates or
+ * frees memory.  All calls share the one array, which keeps the last call's
+ * contents: calls that overlap on the device (different streams without
+ * ordering) race and corrupt each other.  Device-side wait timeouts of these
+ * calls are recorded in the shared scratch and are not reported to the
+ * caller.  Arguments, alignment rules and result are those of agmm_run.
  */
 #define AGMM_STATIC_SCRATCH_BYTES ((size_t)64 << 20) /* 64 MiB */
 agmm_status_t agmm_run_unfused_noalloc(agmm_plan_t plan, const void* const* x_shards, const void* y,

@@ -78,6 +78,36 @@ def check(gpu_out: torch.Tensor, ref32: np.ndarray, tag: str = "") -> dict:
     return stats
 
 
+def check_blocks(gpu_out: torch.Tensor, ref32: np.ndarray, tag: str = "", rows_per_block: int = 1024) -> dict:
+    """The gate of check() over every element of a large output, a block of
+    rows at a time (bounded host memory): the relative Frobenius error is
+    accumulated over all blocks, the per-element bound holds in each."""
+    M = gpu_out.shape[0]
+    assert ref32.shape == tuple(gpu_out.shape), (ref32.shape, tuple(gpu_out.shape))
+    num = den = 0.0
+    max_abs = 0.0
+    for r0 in range(0, M, rows_per_block):
+        r1 = min(M, r0 + rows_per_block)
+        g = gpu_out[r0:r1].float().cpu().numpy().astype(np.float64)
+        r = ref32[r0:r1].astype(np.float64)
+        assert np.all(np.isfinite(g)), f"{tag}: non-finite outputs in rows [{r0}, {r1}) (unwritten rows?)"
+        d = g - r
+        num += float(np.sum(d * d))
+        den += float(np.sum(r * r))
+        err = np.abs(d)
+        max_abs = max(max_abs, float(err.max()))
+        if gpu_out.dtype == torch.float32:
+            assert err.max() <= MAX_ABS, f"{tag}: max abs error {err.max():.3e} > {MAX_ABS} in rows [{r0}, {r1})"
+        else:
+            ulp = f16_ulp(r) if gpu_out.dtype == torch.float16 else bf16_ulp(r)
+            bad = np.argwhere(err > np.maximum(MAX_ABS, ulp))
+            assert bad.size == 0, (f"{tag}: {len(bad)} elements beyond max(2e-2, ulp) in rows [{r0}, {r1}); "
+                                   f"first {(bad[:3] + [r0, 0]).tolist()}")
+    fro = (num ** 0.5) / max(den ** 0.5, 1e-30)
+    assert fro <= REL_FRO, f"{tag}: relative Frobenius error {fro:.3e} > {REL_FRO}"
+    return {"max_abs": max_abs, "rel_fro": fro}
+
+
 def oracle_rows(xs_cpu, y_cpu, rt, rows):
     """Oracle float32 sums of the selected output rows: the selected rows of
     the rank-order concatenation form a one-shard problem for the oracle."""

@@ -8,7 +8,7 @@ import torch
 import oracle
 from all_gather_gemm_agmm_gb300.inputs import WORKLOADS, make_inputs
 
-from parity import alloc_output_guarded, check, guards_intact, oracle_rows, to_device_guarded
+from parity import alloc_output_guarded, check, check_blocks, guards_intact, oracle_rows, to_device_guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -80,13 +80,23 @@ def test_f16_unfused_and_my_id(agmm, case):
         check(o, ref32, f"{case} f16 fused my_id={i}")
 
 
-@pytest.mark.parametrize("name", ["c3_mid", "c4_prefill", "sweep_P8_m1000_rt"])
-def test_f16_full_size_sampled_rows(agmm, name):
+@pytest.mark.parametrize("name", ["c3_mid", "sweep_P8_m1000_rt", "c4_prefill"])
+def test_f16_full_size(agmm, name):
+    # every element of the mid-size workload and a ragged sweep point; on the
+    # prefill-like workload one random row of every 128 output rows (every
+    # row tile) and each shard's first, middle and last rows
     w = WORKLOADS[name]
     xs_cpu, y_cpu = make_inputs(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, w.dist, w.seed, dtype="f16")
     o, plan = _run(agmm, xs_cpu, y_cpu, w.rhs_transpose, my_id=w.my_id)
+    if name != "c4_prefill":
+        ref32, _ = oracle.agmm(xs_cpu, y_cpu, w.rhs_transpose)
+        check_blocks(o, ref32, f"{name} f16 {plan.info()}")
+        return
     rng = np.random.default_rng(3)
-    rows = sorted(set(int(v) for v in rng.integers(0, w.M, size=24)) | {0, w.M - 1, w.m_per_device // 2})
+    rows = {int(t + rng.integers(0, min(128, w.M - t))) for t in range(0, w.M, 128)}
+    for r in range(w.P):
+        rows |= {r * w.m_per_device, r * w.m_per_device + w.m_per_device // 2, (r + 1) * w.m_per_device - 1}
+    rows = sorted(rows)
     ref = oracle_rows(xs_cpu, y_cpu, w.rhs_transpose, rows)
     idx = torch.tensor(rows, device=o.device)
     check(o.index_select(0, idx), ref, f"{name} f16 {plan.info()}")

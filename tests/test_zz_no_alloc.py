@@ -1,12 +1,13 @@
 """The allocation-free entry point agmm_run_unfused_noalloc.
 
 It serves callers that cannot allocate device memory where they run the
-all-gather matmul (inside CUDA graph capture, under an allocator that owns all
-device memory, or in loops that cannot afford cudaMalloc's synchronisation):
-its scratch is a static device array inside the library.  These tests call it
-through the C ABI, twice in a row on the same static scratch, and compare its
-output with agmm_run_unfused on a caller workspace.  This file is collected
-last so that a run stopping at the first failure has run every other test.
+all-gather matmul: code under a framework allocator that has reserved the
+device's memory for itself, and loops that cannot afford the implicit device
+synchronisation of cudaMalloc and cudaFree.  Its scratch is a static device
+array inside the library.  These tests call it through the C ABI, twice in a
+row on the same static scratch, and compare its output with agmm_run_unfused
+on a caller workspace and with the CPU oracle.  This file is collected last
+so that a run stopping at the first failure has run every other test.
 """
 import ctypes
 
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from all_gather_gemm_agmm_gb300.inputs import make_inputs
 
 from parity import check
@@ -54,13 +56,15 @@ def test_noalloc_matches_unfused_twice(agmm, case):
     plan.run_unfused(xs, y, o_ref, P - 1, plan.new_workspace(True))
     torch.cuda.synchronize()
     ref = o_ref.float().cpu().numpy()
+    ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
     for call in range(2):
         o = torch.full((P * m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
         rc = lib.agmm_run_unfused_noalloc(plan._h, _ptrs(xs), y.data_ptr(), o.data_ptr(), P - 1,
                                           stream.cuda_stream)
         assert rc == agmm.AGMM_OK, lib.agmm_last_error().decode()
         torch.cuda.synchronize()
-        check(o, ref, f"no-alloc call {call}")
+        check(o, ref, f"no-alloc call {call} vs agmm_run_unfused")
+        check(o, ref32, f"no-alloc call {call} vs the oracle")
 
 
 def test_noalloc_rejects_oversized_problem(agmm):
