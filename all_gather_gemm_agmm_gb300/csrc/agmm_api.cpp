@@ -155,7 +155,6 @@ struct agmm_plan_s {
   const void* cache_xcat = nullptr;  // buffer the gathered-LHS maps describe
   KernelParams params{};
   agmm_plan_s* sub = nullptr;  // unfused path: P = 1 over the gathered buffer
-  agmm_plan_s* gather = nullptr;  // CTA-pair plans: the same tiles without the pair, for agmm_run_gather
   agmm_tile_config_t user_cfg{};  // the caller's configuration (fields 0 when none)
   size_t out_elem = 2;
   int64_t M() const { return (int64_t)P * m_pd; }
@@ -610,6 +609,16 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       return fail_cuda(e, "kernel attribute setup");
     }
     if (pl->key.path == kPathRows) {
+      // the variant with the gathered-LHS store warp runs on the same grid
+      KernelKey sk = pl->key;
+      sk.store = true;
+      int active_store = 0;
+      e = prepare_agmm_kernel(sk, pl->smem_bytes, cluster, &active_store);
+      if (e != cudaSuccess) {
+        delete pl;
+        return fail_cuda(e, "kernel attribute setup (store variant)");
+      }
+      active = std::min(active, active_store);
       if (active <= 0) {
         delete pl;
         return fail(AGMM_ERR_UNSUPPORTED, "row kernel cannot be resident");
@@ -672,17 +681,6 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       return st;
     }
   }
-  if (with_sub && pl->key.pair) {
-    agmm_tile_config_t gc = pl->user_cfg;
-    gc.cta_pair = AGMM_CFG_OFF;
-    gc.cluster_m = 1;
-    st = plan_impl(P, m_pd, k, n, dtype, rhs_t, &gc, false, &pl->gather);
-    if (st != AGMM_OK) {
-      agmm_destroy(pl->sub);
-      delete pl;
-      return st;
-    }
-  }
   *out = pl;
   return AGMM_OK;
 }
@@ -717,7 +715,8 @@ agmm_status_t check_run_args(agmm_plan_s* pl, const void* const* xs, const void*
 agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y, void* o, int my_id,
                            void* status, void* tail_ws, cudaStream_t stream, void* xcat = nullptr) {
   KernelParams& kpx = pl->params;
-  kpx.store_xcat = xcat != nullptr ? 1 : 0;
+  // swapped tiles: the MMA thread stores the X boxes when asked
+  kpx.store_xcat = xcat != nullptr && pl->key.path == kPathSwap ? 1 : 0;
   if (xcat != nullptr && xcat != pl->cache_xcat) {
     // per-shard views of the gathered buffer: a store is clipped at its shard
     std::string err;
@@ -782,11 +781,14 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
     kp.sk_flags = nullptr;
     kp.sk_partials = nullptr;
   }
+  // Row tiles writing the gathered LHS run the variant with the store warp.
+  KernelKey key = pl->key;
+  key.store = xcat != nullptr && pl->key.path == kPathRows;
   // Stream-K owners wait for other CTAs.  Without clusters a cooperative
   // launch guarantees that every CTA of the grid is resident at once; with
   // clusters the planner sized the grid to the co-resident cluster count, and
   // the owners' waits are bounded in any case.
-  cudaError_t e = launch_agmm_kernel(pl->key, kp, pl->grid, pl->cluster_x, pl->smem_bytes,
+  cudaError_t e = launch_agmm_kernel(key, kp, pl->grid, pl->cluster_x, pl->smem_bytes,
                                      pl->sk_tiles > 0 && pl->cluster_x == 1, stream);
   if (e != cudaSuccess) return fail_cuda(e, "fused kernel launch");
   return AGMM_OK;
@@ -858,14 +860,12 @@ agmm_status_t agmm_plan(int P, int64_t m_per_device, int64_t k, int64_t n, agmm_
 void agmm_destroy(agmm_plan_t plan) {
   if (!plan) return;
   agmm_destroy(plan->sub);
-  agmm_destroy(plan->gather);
   delete plan;
 }
 
 size_t agmm_workspace_bytes(agmm_plan_t plan, int unfused) {
   if (!plan) return 0;
-  if (!unfused || plan->P == 1)
-    return kStatusBytes + std::max(plan->tail_bytes, plan->gather ? plan->gather->tail_bytes : (size_t)0);
+  if (!unfused || plan->P == 1) return kStatusBytes + plan->tail_bytes;
   return kStatusBytes + gathered_bytes(plan) + plan->sub->tail_bytes;
 }
 
@@ -891,11 +891,7 @@ agmm_status_t agmm_run_gather(agmm_plan_t plan, const void* const* x_shards, con
       overlaps(o, (size_t)plan->M() * plan->n * plan->out_elem, xcat, gbytes) ||
       overlaps(workspace, agmm_workspace_bytes(plan, 0), xcat, gbytes))
     return fail(AGMM_ERR_INVALID_ARG, "xcat overlaps Y, O or the workspace");
-  // the CTA-pair kernel does not store X boxes: run the plan's companion
-  agmm_plan_s* run = plan->key.pair ? plan->gather : plan;
-  if (!run) return fail(AGMM_ERR_UNSUPPORTED, "no plan without the CTA pair for the gathered LHS");
-  run->params.trace = plan->params.trace;
-  return launch_fused(run, x_shards, y, o, my_id, workspace, static_cast<uint8_t*>(workspace) + kStatusBytes,
+  return launch_fused(plan, x_shards, y, o, my_id, workspace, static_cast<uint8_t*>(workspace) + kStatusBytes,
                       static_cast<cudaStream_t>(stream), xcat);
 }
 
@@ -961,8 +957,8 @@ agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream)
     return fail_cuda(e, "status read");
   if (words[0] == 0) return AGMM_OK;
   if ((e = cudaMemset(workspace, 0, sizeof words)) != cudaSuccess) return fail_cuda(e, "status clear");
-  static const char* roles[] = {"?", "producer", "mma", "epilogue", "drain"};
-  const char* role = (words[1] >= 1 && words[1] <= 4) ? roles[words[1]] : roles[0];
+  static const char* roles[] = {"?", "producer", "mma", "epilogue", "drain", "store"};
+  const char* role = (words[1] >= 1 && words[1] <= 5) ? roles[words[1]] : roles[0];
   return fail(words[0] == AGMM_ERR_TIMEOUT ? AGMM_ERR_TIMEOUT : AGMM_ERR_CUDA,
               std::string("device wait ran out in the ") + role + " role (stage " + std::to_string(words[2]) +
                   ", tile " + std::to_string(words[3]) + "; detail " + std::to_string(words[4]) + " " +
@@ -971,8 +967,7 @@ agmm_status_t agmm_query_status(agmm_plan_t plan, void* workspace, void* stream)
 
 size_t agmm_trace_bytes(agmm_plan_t plan) {
   if (!plan) return 0;
-  size_t ctas = (size_t)plan->grid.x * plan->grid.y * plan->grid.z;
-  if (plan->gather) ctas = std::max(ctas, (size_t)plan->gather->grid.x * plan->gather->grid.y * plan->gather->grid.z);
+  const size_t ctas = (size_t)plan->grid.x * plan->grid.y * plan->grid.z;
   return ctas * kTraceSlots * sizeof(uint64_t);
 }
 

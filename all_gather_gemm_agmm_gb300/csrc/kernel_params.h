@@ -11,6 +11,8 @@ namespace agmm {
 constexpr int kMaxShards = 8;
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 192;       // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
+constexpr int kThreadsStore = 224;  // row tiles storing the gathered LHS: + warp 6, the store warp
+constexpr int kStoreWarp = 6;
 constexpr int kTileM = 128;         // MMA M (one CTA, 128 TMEM lanes)
 constexpr int kTileK = 64;          // k per stage: one 128-byte swizzle row of bf16
 constexpr int kASlotBytes = kTileM * kTileK * 2;  // 16 KiB
@@ -24,7 +26,7 @@ enum Path : int { kPathRows = 0, kPathSwap = 1 };
 
 // Status word layout (int32 at the workspace base):
 //   [0] first error code (0 = none), [1] role that gave up, [2] stage, [3] tile.
-enum StatusRole : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
+enum StatusRole : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4, kRoleStore = 5 };
 
 struct __align__(128) KernelParams {
   CUtensorMap xmap[kMaxShards];  // shard r: [m_pd, k] bf16, box {64, box_rows}, 128B swizzle
@@ -75,8 +77,9 @@ struct __align__(128) KernelParams {
   int f16;  // X, Y and a 16-bit O are fp16 (else bf16)
   // Optional by-product: the gathered LHS.  xcatmap[r] views rows
   // [r*m_pd, (r+1)*m_pd) of the caller's [P*m_pd, k] buffer with the shard
-  // maps' box; with store_xcat each X box is stored there once, by the n
-  // tile whose share of the k range holds it.
+  // maps' box; each X box is stored there once, by the n tile whose share of
+  // the k range holds it (swapped tiles: the MMA thread, when store_xcat is
+  // set; row tiles: the store warp of the KernelKey::store variant).
   CUtensorMap xcatmap[kMaxShards];
   int store_xcat;
   int y3d;                       // Y [k, n]: one 3-D box per load instead of one 2-D box per 64 columns
@@ -99,6 +102,8 @@ struct KernelKey {
   bool pair;  // cm == 2: one cta_group::2 MMA per pair, each CTA holding half the Y tile
               // (a two-CTA cluster is always a pair; no copy is multicast)
   int atoms = 1;  // swap path: k blocks per pipeline stage (1 or 2)
+  bool store = false;  // row path: the variant with a store warp that writes the
+                       // landed X boxes to the gathered LHS (agmm_run_gather)
 };
 
 // Largest dynamic shared memory a CTA may request (227 KiB on sm_100-class parts).

@@ -602,6 +602,26 @@ def bench_sweep(args):
         torch.cuda.empty_cache()
 
 
+def bench_profile_target(args, w):
+    """A plain run for profilers: W warm-up launches, then K launches of one
+    path (--path fused | unfused | gather) over the workload's replicas, eager
+    (no CUDA graph), then a status check.  Prints nothing timed: a number
+    taken under a profiler is not a benchmark value."""
+    import torch
+
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=device)
+    wb = WorkloadBench(w, device, args.dtype)
+    fns = {"fused": wb.fused, "unfused": wb.unfused, "gather": wb.gathered}[args.path]()
+    for i in range(args.warmup + args.steps):
+        fns[i % len(fns)](stream.cuda_stream)
+    wb.plan.query_status(wb.ws_unf if args.path == "unfused" else wb.ws, stream)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_target": w.name, "path": args.path, "launches": args.warmup + args.steps,
+                      "replicas": wb.R, "plan": wb.plan.info()}), flush=True)
+
+
 # ----------------------------------------------------------------------------- reference arm
 def bench_reference(args, w):
     """The oracle as it stands, on the host cores, on bounded samples of the
@@ -656,6 +676,9 @@ def main(argv=None):
     ap.add_argument("--sub", default="c2_decode,c3_mid",
                     help="comma-separated workloads measured as sub-results of the same line")
     ap.add_argument("--sweep-points", default="", help="with --sweep: comma-separated sweep point names")
+    ap.add_argument("--profile-target", action="store_true",
+                    help="only launch W + K steps of --path, eagerly, for a profiler (no timing)")
+    ap.add_argument("--path", choices=["fused", "unfused", "gather"], default="fused")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="element type of X, Y and O (fp16: the tutorial's float16 variant)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -671,6 +694,8 @@ def main(argv=None):
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         bench_reference(args, w)
+    elif args.profile_target:
+        bench_profile_target(args, w)
     elif args.sweep:
         bench_sweep(args)
     else:

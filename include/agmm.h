@@ -221,11 +221,11 @@ agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void
  * Each X box is stored straight from shared memory (TMA) by one of the CTAs
  * that load it: n tile t stores the k blocks in the t-th share of the k
  * range, so the gathered rows are written once, never read back, and the
- * store work is spread over all n tiles.  xcat must not overlap the shards, Y, O or the workspace
- * (AGMM_ERR_INVALID_ARG).  The CTA-pair row kernel does not store the
- * gathered rows: a plan that uses it runs this call through a companion plan
- * of the same tiles without the pair (built with the plan, covered by
- * agmm_workspace_bytes(plan, 0)).
+ * store work is spread over all n tiles.  On row tiles a dedicated store warp
+ * issues the stores while the MMAs read the same stage (a CTA pair's two CTAs
+ * each store their own rows); on swapped tiles the MMA thread does.  xcat
+ * must not overlap the shards, Y, O or the workspace (AGMM_ERR_INVALID_ARG).
+ * The workspace is agmm_workspace_bytes(plan, 0) bytes, as for agmm_run.
  */
 agmm_status_t agmm_run_gather(agmm_plan_t plan, const void* const* x_shards, const void* y, void* o, void* xcat,
                               int my_id, void* workspace, void* stream);

@@ -124,8 +124,8 @@ def test_gathered_lhs_argument_errors_and_pair_plans(agmm):
     with pytest.raises(agmm.AgmmError) as err:
         plan.run_gather(xs, y, o, xs[0], 0, ws)
     assert err.value.status == agmm.AGMM_ERR_INVALID_ARG
-    # a CTA-pair plan (the row-tile default for two-CTA clusters) runs this
-    # call through its companion plan without the pair
+    # a CTA-pair plan (the row-tile default): each CTA's store warp writes
+    # its own rows
     pm, pk, pn = 256, 512, 256
     xs2, y2 = make_inputs(2, pm, pk, pn, False, seed=17)
     pplan = agmm.Plan(2, pm, pk, pn, False, config={"path": "rows", "cluster_m": 2, "cta_pair": True})
@@ -140,3 +140,47 @@ def test_gathered_lhs_argument_errors_and_pair_plans(agmm):
     assert torch.equal(xc.cpu().view(torch.int16), torch.cat(xs2).view(torch.int16))
     ref32, _ = oracle.agmm(xs2, y2, False)
     check(o2, ref32, "CTA-pair plan with gathered LHS")
+
+
+ROW_FORMS = [
+    {"path": "rows"},                                   # CTA pairs (the default)
+    {"path": "rows", "cluster_m": 1},                   # one CTA per cluster
+    {"path": "rows", "stages": 2},                      # a short ring: refills wait on the stores
+    {"path": "rows", "stream_k": True, "group_m": 3},   # k blocks of the last wave shared
+]
+ROW_SHAPES = [
+    (4, 512, 1024, 4096, True),    # 16 row tiles x 16 n tiles: several tiles per cluster, 1 k block stored per tile
+    (3, 200, 2048, 384, False),    # ragged halves, odd row-tile count (an idle pair follower)
+    (5, 77, 768, 1280, True),      # odd shards, 5 n tiles of 256
+]
+
+
+@pytest.mark.parametrize("cfg", ROW_FORMS, ids=str)
+@pytest.mark.parametrize("shape", ROW_SHAPES, ids=lambda c: "P{}_m{}_k{}_n{}".format(*c[:4]))
+def test_gathered_lhs_row_tile_forms(agmm, cfg, shape):
+    # Row tiles store the gathered LHS from a store warp in each CTA while the
+    # MMAs read the same stage; the gathered buffer is exact and O is bitwise
+    # the plain run's O under the same plan.
+    P, m, k, n, rt = shape
+    xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=18)
+    plan = agmm.Plan(P, m, k, n, rt, config=cfg)
+    info = plan.info()
+    assert info["path"] == 0
+    xs = [to_device_guarded(x)[0] for x in xs_cpu]
+    y, _ = to_device_guarded(y_cpu)
+    o_g, obuf = alloc_output_guarded(P * m, n)
+    xcat, xbuf = alloc_output_guarded(P * m, k)
+    o = torch.empty_like(o_g)
+    ws = plan.new_workspace()
+    torch.cuda.synchronize()
+    for _ in range(2):  # a second run on the same workspace
+        plan.run_gather(xs, y, o_g, xcat, P - 1, ws)
+        plan.query_status(ws)
+    plan.run(xs, y, o, P - 1, ws)
+    plan.query_status(ws)
+    torch.cuda.synchronize()
+    assert guards_intact(obuf) and guards_intact(xbuf), info
+    assert torch.equal(xcat.cpu().view(torch.int16), torch.cat(xs_cpu).view(torch.int16)), info
+    assert torch.equal(o.view(torch.int16), o_g.view(torch.int16)), info
+    ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+    check(o_g, ref32, f"{shape} {cfg} {info}")
