@@ -609,7 +609,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       return fail_cuda(e, "kernel attribute setup");
     }
     if (pl->key.path == kPathRows) {
-      // the variant with the gathered-LHS store warp runs on the same grid
+      // the variant that also copies the gathered LHS runs on the same grid
       KernelKey sk = pl->key;
       sk.store = true;
       int active_store = 0;
@@ -715,8 +715,12 @@ agmm_status_t check_run_args(agmm_plan_s* pl, const void* const* xs, const void*
 agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y, void* o, int my_id,
                            void* status, void* tail_ws, cudaStream_t stream, void* xcat = nullptr) {
   KernelParams& kpx = pl->params;
-  // swapped tiles: the MMA thread stores the X boxes when asked
+  // swapped tiles: the MMA thread stores the X boxes when asked; row tiles:
+  // the store warp of the store variant writes them to xcat
   kpx.store_xcat = xcat != nullptr && pl->key.path == kPathSwap ? 1 : 0;
+  kpx.xcat = xcat;
+  kpx.ldx = pl->k;
+  for (int r = 0; r < kMaxShards; ++r) kpx.xsrc[r] = r < pl->P ? xs[r] : nullptr;
   if (xcat != nullptr && xcat != pl->cache_xcat) {
     // per-shard views of the gathered buffer: a store is clipped at its shard
     std::string err;
@@ -781,7 +785,7 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
     kp.sk_flags = nullptr;
     kp.sk_partials = nullptr;
   }
-  // Row tiles writing the gathered LHS run the variant with the store warp.
+  // Row tiles writing the gathered LHS run the variant whose epilogue copies it.
   KernelKey key = pl->key;
   key.store = xcat != nullptr && pl->key.path == kPathRows;
   // Stream-K owners wait for other CTAs.  Without clusters a cooperative

@@ -15,10 +15,9 @@
 //               tiles it also TMA-stores the landed X boxes to a gathered-LHS
 //               buffer before releasing each stage, when asked;
 //   warps 2-5   drain TMEM with tcgen05.ld, round to the output dtype and store
-//               each row at its rank-order offset;
-//   warp 6      (row tiles writing the gathered LHS only) TMA-stores each
-//               landed X box of this CTA's rows; the stage is refilled only
-//               once both the MMA and that store have read it.
+//               each row at its rank-order offset; on row tiles writing the
+//               gathered LHS they also copy a share of each tile's X rows to it
+//               while the tile's main loop runs (the ring is not involved).
 // Issuing from converged warps keeps the copy and MMA operands warp-uniform;
 // a loop that a single lane runs alone pays for moving them to uniform
 // registers at every issue.  Both loops test the next stage's barrier while
@@ -72,18 +71,7 @@ __device__ __forceinline__ uint32_t bar_drain(uint32_t ctl) {
 // (1 arrival) and the contributors' "partial stored" (128 arrivals).
 __device__ __forceinline__ uint32_t bar_owner_go(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 5); }
 __device__ __forceinline__ uint32_t bar_published(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 6); }
-// Gathered-LHS store warp (row tiles), one phase per store use of stage s:
-//   sarm(s)   the producer has issued a stored k block's copies into stage s
-//             (1 arrival; leader or lone CTA), so the stage's full barrier is
-//             in that use's phase;
-//   xready(s) stage s has landed in both CTAs of a pair (1 arrival, from the
-//             leader's store warp to the follower's);
-//   sfree(s)  this CTA's store of stage s has finished reading it (1 arrival,
-//             from its store warp to its producer).
-__device__ __forceinline__ uint32_t bar_xready(uint32_t ctl, int s) { return ctl + 8u * (2 * kMaxStages + 7 + s); }
-__device__ __forceinline__ uint32_t bar_sfree(uint32_t ctl, int s) { return ctl + 8u * (3 * kMaxStages + 7 + s); }
-__device__ __forceinline__ uint32_t bar_sarm(uint32_t ctl, int s) { return ctl + 8u * (4 * kMaxStages + 7 + s); }
-constexpr int kAbortOffset = 8 * (5 * kMaxStages + 8);  // int
+constexpr int kAbortOffset = 8 * (3 * kMaxStages + 7);  // int
 constexpr int kTmemOffset = kAbortOffset + 16;          // uint32
 constexpr int kChunkTabOffset = 512;                    // int4[kMaxSwapChunks]: shard, src_row, valid, out_row
 static_assert(kTmemOffset + 4 <= kChunkTabOffset, "control block overlap");
@@ -366,19 +354,71 @@ __device__ __forceinline__ void owner_sum_global(const KernelParams& p, const Ow
   }
 }
 
+// Row tiles writing the gathered LHS: the epilogue warps (128 threads, t =
+// 0..127) copy k blocks [kb_a, kb_b) of row tile mt's X rows from the shards
+// to their rows of the gathered LHS, 16 bytes per load and store.  Each n
+// tile copies its own share of the k blocks, so every (row, k block) is
+// written once; the copy reads the shards directly (mostly from L2, where the
+// main loop is streaming the same rows) and never touches the shared-memory
+// ring.
+__device__ __noinline__ void copy_x_rows(const KernelParams& p, const RingGeom& geom, int mt, int kb_a, int kb_b,
+                                         int lane, int t) {
+  if (kb_b <= kb_a || mt >= p.num_m_tiles) return;
+  const int cpt = kTileM / p.box_rows;
+  // lane j < cpt holds chunk j of the row tile (valid 0: none)
+  int shard = 0, valid = 0;
+  int64_t src_row = 0, out_row = 0;
+  if (lane < cpt && (int64_t)mt * cpt + lane < p.total_chunks) {
+    const RingChunk ch = ring_chunk(geom, (int64_t)mt * cpt + lane);
+    shard = ch.shard;
+    valid = ch.valid;
+    src_row = ch.src_row;
+    out_row = ch.out_row;
+  }
+  const int ppr = (kb_b - kb_a) * (kTileK / 8);  // 16-byte pieces per row
+  const int64_t col0 = (int64_t)kb_a * kTileK;
+  const int units = kTileM * ppr;
+  uint16_t* const xcat = static_cast<uint16_t*>(p.xcat);
+  constexpr int U = 8;  // loads in flight per thread
+  for (int base = 0; base < units; base += 128 * U) {
+    uint4 v[U];
+    int64_t dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int idx = base + u * 128 + t;
+      const int r = min(idx / ppr, kTileM - 1);
+      const int pc = idx - r * ppr;
+      const int j = r >> p.box_shift;
+      const int rr = r & (p.box_rows - 1);
+      const int sh = __shfl_sync(0xffffffffu, shard, j);
+      const int vl = __shfl_sync(0xffffffffu, valid, j);
+      const int64_t sr = __shfl_sync(0xffffffffu, src_row, j);
+      const int64_t orow = __shfl_sync(0xffffffffu, out_row, j);
+      dst[u] = -1;
+      if (idx < units && rr < vl) {
+        const int64_t c = col0 + (int64_t)pc * 8;
+        v[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.xsrc[sh]) + (sr + rr) * p.ldx + c));
+        dst[u] = (orow + rr) * p.ldx + c;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (dst[u] >= 0) *reinterpret_cast<uint4*>(xcat + dst[u]) = v[u];
+  }
+}
+
 // ----------------------------------------------------------------------------
 // The fused kernel.  kPath: kPathRows / kPathSwap.  kYK: Y stored [n, k]
 // (K-major tiles); otherwise Y is [k, n] and its tiles are MN-major.  kF32:
 // float32 output.  kBN: n tile of the rows path (the swap path uses 128).
 // ----------------------------------------------------------------------------
 template <int kPath, bool kYK, bool kF32, int kBN, int kCM, bool kPair, int kAtoms, bool kStore>
-__global__ void __launch_bounds__(kStore ? kThreadsStore : kThreads, 1)
-    agmm_fused_sm103a(const __grid_constant__ KernelParams p) {
+__global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_constant__ KernelParams p) {
   // Clusters exist only as CTA pairs of the rows path: no copy is multicast.
   static_assert(kCM == 1 || (kCM == 2 && kPair), "two-CTA clusters multiply as a CTA pair");
   static_assert(!kPair || (kCM == 2 && kPath == kPathRows), "CTA pairs are clusters of two on the rows path");
   static_assert(kAtoms == 1 || (kAtoms == 2 && kPath == kPathSwap), "two k blocks per stage: swapped tiles");
-  static_assert(!kStore || kPath == kPathRows, "the store warp serves row tiles");
+  static_assert(!kStore || kPath == kPathRows, "the epilogue's copy of the gathered LHS serves row tiles");
   // The leader's accumulator-release barrier receives the follower's
   // epilogue arrivals (release at cluster scope): its wait acquires at
   // cluster scope.  Stage barriers are fed by TMA and tcgen05.commit.
@@ -423,13 +463,6 @@ __global__ void __launch_bounds__(kStore ? kThreadsStore : kThreads, 1)
       ptx::mbar_init(bar_acc_full(ctl, a), 1);
       // a pair: both CTAs' epilogues drain the accumulator the leader fills
       ptx::mbar_init(bar_acc_empty(ctl, a), kPair ? 256 : 128);
-    }
-    if constexpr (kStore) {
-      for (int s = 0; s < S; ++s) {
-        ptx::mbar_init(bar_xready(ctl, s), 1);
-        ptx::mbar_init(bar_sfree(ctl, s), 1);
-        ptx::mbar_init(bar_sarm(ctl, s), 1);
-      }
     }
     ptx::mbar_init(bar_drain(ctl), 1);
     ptx::mbar_init(bar_owner_go(ctl), 1);
@@ -513,9 +546,6 @@ __global__ void __launch_bounds__(kStore ? kThreadsStore : kThreads, 1)
       SegmentIter iter;
       iter.init(p, cluster_id, nclusters);
       bool swap_pending = true;
-      // store warp: stages whose gathered-LHS store may still be reading
-      // them, and the parity of each stage's next sfree phase
-      uint32_t sfree_pend = 0, sfree_par = 0;
       for (int tile = 0; ok; ++tile) {
         int mt = 0, nt = swap_nt;
         int kb0 = kb_begin, kb1 = kb_end;
@@ -550,9 +580,6 @@ __global__ void __launch_bounds__(kStore ? kThreadsStore : kThreads, 1)
         // kept in registers rather than the chunk arrays.
         const CUtensorMap* xmap0 = (kPath == kPathRows && nchunks > 0) ? &p.xmap[shard_j[0]] : nullptr;
         const int xrow0 = (kPath == kPathRows && nchunks > 0) ? row_j[0] : 0;
-        // k blocks [st_lo, st_hi) of this n tile are stored by the store warp
-        const int st_lo = kStore ? (int)((int64_t)nt * p.num_k_blocks / p.num_n_tiles) : 0;
-        const int st_hi = kStore ? (int)((int64_t)(nt + 1) * p.num_k_blocks / p.num_n_tiles) : 0;
         // The next stage's empty barrier is tested while this stage's copies
         // are issued, so its latency is off the loop's critical path.
         bool empty_ready = false;
@@ -566,21 +593,6 @@ __global__ void __launch_bounds__(kStore ? kThreadsStore : kThreads, 1)
               ok = false;
               break;
             }
-          }
-          if constexpr (kStore) {
-            // the store of this stage's previous X boxes must have read them
-            if ((sfree_pend >> stage) & 1u) {
-              int sres = wait_phase(bar_sfree(ctl, stage), (sfree_par >> stage) & 1u, abort_flag, limit);
-              sres = __shfl_sync(0xffffffffu, sres, 0);
-              if (sres != kWaitOk) {
-                if (leader) record_failure(p, abort_flag, sres, kRoleProducer, stage, tile);
-                ok = false;
-                break;
-              }
-              sfree_par ^= 1u << stage;
-              sfree_pend &= ~(1u << stage);
-            }
-            if (kb >= st_lo && kb < st_hi) sfree_pend |= 1u << stage;
           }
           const int next_stage = (stage + 1 == S) ? 0 : stage + 1;
           const uint32_t next_phase = (stage + 1 == S) ? (phase ^ 1u) : phase;
@@ -678,10 +690,6 @@ __global__ void __launch_bounds__(kStore ? kThreadsStore : kThreads, 1)
               }
             }
             }  // k blocks of the stage
-          }
-          if constexpr (kStore) {
-            // (after this stage's arrive.expect_tx, in the same thread)
-            if (leader && !(kPair && crank == 1) && kb >= st_lo && kb < st_hi) ptx::mbar_arrive(bar_sarm(ctl, stage));
           }
           if (!traced_first) {
             trace(p, 2);
@@ -862,78 +870,6 @@ __global__ void __launch_bounds__(kStore ? kThreadsStore : kThreads, 1)
       trace(p, 5);
       __syncwarp();
     }
-  } else if (kStore && warp == kStoreWarp) {
-    // ------------------------------------------------------------ store warp
-    // Each n tile stores the k blocks [t*K/T, (t+1)*K/T) of its rows' X
-    // boxes (T n tiles, K k blocks), so every (rows, k block) of the gathered
-    // LHS is written once and the stores spread over all tiles.  The leader
-    // (or a lone CTA) learns that a stored k block's stage has landed from
-    // its full barrier, after sarm has told it that the barrier is in that
-    // use's phase (this warp skips the other k blocks, so it may run ahead of
-    // the ring); the stage cannot be refilled before this warp frees it
-    // (sfree), so the barrier cannot run ahead either.  A pair follower's
-    // copies complete on the leader's barrier, so the leader's store warp
-    // passes the news on (xready).  The MMA and the stores read a stage
-    // concurrently.
-    const bool lead = !kPair || crank == 0;
-    const bool issuer = ptx::elect_one();
-    const int cpt = kTileM / p.box_rows;
-    const uint32_t chunk_bytes = (uint32_t)p.box_rows * 128u;
-    int stage = 0;
-    uint32_t phase = 0, xr_par = 0, sarm_par = 0;
-    SegmentIter iter;
-    iter.init(p, cluster_id, nclusters);
-    bool ok = true;
-    for (int tile = 0; ok; ++tile) {
-      Segment sg;
-      if (!iter.next(p, kCM, crank, sg)) break;
-      const int st_lo = (int)((int64_t)sg.nt * p.num_k_blocks / p.num_n_tiles);
-      const int st_hi = (int)((int64_t)(sg.nt + 1) * p.num_k_blocks / p.num_n_tiles);
-      const bool rows_ok = sg.mt < p.num_m_tiles;
-      for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-        if (kb >= st_lo && kb < st_hi) {
-          int res;
-          if (lead) {
-            res = wait_phase(bar_sarm(ctl, stage), (sarm_par >> stage) & 1u, abort_flag, limit);
-            sarm_par ^= 1u << stage;
-            if (__shfl_sync(0xffffffffu, res, 0) == kWaitOk) res = wait_phase(bar_full(ctl, stage), phase, abort_flag, limit);
-          } else {
-            res = wait_phase<true>(bar_xready(ctl, stage), (xr_par >> stage) & 1u, abort_flag, limit);
-          }
-          res = __shfl_sync(0xffffffffu, res, 0);
-          if (res != kWaitOk) {
-            if (issuer) record_failure(p, abort_flag, res, kRoleStore, stage, tile);
-            ok = false;
-            break;
-          }
-          if (!lead) xr_par ^= 1u << stage;
-          if (issuer) {
-            if (kPair && lead) ptx::mbar_arrive_remote(ptx::map_shared_rank(bar_xready(ctl, stage), 1));
-            if (rows_ok) {
-              const uint32_t a_addr = a0 + (uint32_t)stage * a_slot;
-              for (int j = 0; j < cpt; ++j) {
-                const int64_t gc = (int64_t)sg.mt * cpt + j;
-                if (gc < p.total_chunks) {
-                  const RingChunk ch = ring_chunk(geom, gc);
-                  ptx::tma_store_2d(&p.xcatmap[ch.shard], a_addr + (uint32_t)j * chunk_bytes, kb * kTileK,
-                                    (int)ch.src_row);
-                }
-              }
-              ptx::bulk_commit();
-              ptx::bulk_wait_read_all();
-            }
-            ptx::mbar_arrive(bar_sfree(ctl, stage));
-          }
-          __syncwarp();
-        }
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    if (issuer) ptx::bulk_wait_all();
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -951,6 +887,12 @@ __global__ void __launch_bounds__(kStore ? kThreadsStore : kThreads, 1)
       for (int tile = 0;; ++tile, ++it) {
         Segment sg;
         if (!iter.next(p, kCM, crank, sg)) break;
+        if constexpr (kStore) {
+          // while this segment's main loop runs: its share of the gathered LHS
+          const int st_lo = (int)((int64_t)sg.nt * p.num_k_blocks / p.num_n_tiles);
+          const int st_hi = (int)((int64_t)(sg.nt + 1) * p.num_k_blocks / p.num_n_tiles);
+          copy_x_rows(p, geom, sg.mt, max(st_lo, sg.kb0), min(st_hi, sg.kb1), lane, trow);
+        }
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         int res = kWaitOk;
@@ -1342,7 +1284,7 @@ cudaError_t prepare_agmm_kernel(const KernelKey& key, size_t smem_bytes, int clu
     if (cluster_x > 1) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)cluster_x, 1, 1);
-      cfg.blockDim = dim3(key.store ? kThreadsStore : kThreads, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
       cfg.dynamicSmemBytes = smem_bytes;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1353,8 +1295,7 @@ cudaError_t prepare_agmm_kernel(const KernelKey& key, size_t smem_bytes, int clu
       cfg.numAttrs = 1;
       e = cudaOccupancyMaxActiveClusters(max_active, fn, &cfg);
     } else {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(max_active, fn, key.store ? kThreadsStore : kThreads,
-                                                        smem_bytes);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(max_active, fn, kThreads, smem_bytes);
     }
   }
   return e;
@@ -1366,7 +1307,7 @@ cudaError_t launch_agmm_kernel(const KernelKey& key, const KernelParams& p, dim3
   if (!fn) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(key.store ? kThreadsStore : kThreads, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[3];

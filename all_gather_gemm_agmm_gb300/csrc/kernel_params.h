@@ -11,8 +11,6 @@ namespace agmm {
 constexpr int kMaxShards = 8;
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 192;       // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
-constexpr int kThreadsStore = 224;  // row tiles storing the gathered LHS: + warp 6, the store warp
-constexpr int kStoreWarp = 6;
 constexpr int kTileM = 128;         // MMA M (one CTA, 128 TMEM lanes)
 constexpr int kTileK = 64;          // k per stage: one 128-byte swizzle row of bf16
 constexpr int kASlotBytes = kTileM * kTileK * 2;  // 16 KiB
@@ -78,11 +76,15 @@ struct __align__(128) KernelParams {
   // Optional by-product: the gathered LHS.  xcatmap[r] views rows
   // [r*m_pd, (r+1)*m_pd) of the caller's [P*m_pd, k] buffer with the shard
   // maps' box; each X box is stored there once, by the n tile whose share of
-  // the k range holds it (swapped tiles: the MMA thread, when store_xcat is
-  // set; row tiles: the store warp of the KernelKey::store variant).
+  // the k range holds it (swapped tiles: the MMA thread TMA-stores the landed
+  // boxes when store_xcat is set; row tiles: the epilogue warps of the
+  // KernelKey::store variant copy them from the shards, see xcat below).
   CUtensorMap xcatmap[kMaxShards];
   int store_xcat;
   int y3d;                       // Y [k, n]: one 3-D box per load instead of one 2-D box per 64 columns
+  void* xcat;                    // row tiles: the gathered LHS [P*m_pd, k], written by the epilogue warps
+  int64_t ldx;                   // its row stride and the shards' in elements (= k)
+  const void* xsrc[kMaxShards];  // row tiles: the shards, read by that copy
 };
 
 struct GatherParams {
@@ -102,8 +104,8 @@ struct KernelKey {
   bool pair;  // cm == 2: one cta_group::2 MMA per pair, each CTA holding half the Y tile
               // (a two-CTA cluster is always a pair; no copy is multicast)
   int atoms = 1;  // swap path: k blocks per pipeline stage (1 or 2)
-  bool store = false;  // row path: the variant with a store warp that writes the
-                       // landed X boxes to the gathered LHS (agmm_run_gather)
+  bool store = false;  // row path: the variant whose epilogue warps also copy
+                       // the X rows to the gathered LHS (agmm_run_gather)
 };
 
 // Largest dynamic shared memory a CTA may request (227 KiB on sm_100-class parts).

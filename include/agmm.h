@@ -218,12 +218,12 @@ agmm_status_t agmm_run(agmm_plan_t plan, const void* const* x_shards, const void
  *   xcat  device pointer to [P*m_per_device, k] elements of the input type,
  *         row-major, 16-byte aligned, caller-owned; on return (stream order)
  *         it holds concat(X_0, ..., X_{P-1}) in rank order, bit for bit.
- * Each X box is stored straight from shared memory (TMA) by one of the CTAs
- * that load it: n tile t stores the k blocks in the t-th share of the k
+ * Each (rows, k block) piece is stored by one of the CTAs that load it: n
+ * tile t stores the k blocks in the t-th share of the k
  * range, so the gathered rows are written once, never read back, and the
- * store work is spread over all n tiles.  On row tiles a dedicated store warp
- * issues the stores while the MMAs read the same stage (a CTA pair's two CTAs
- * each store their own rows); on swapped tiles the MMA thread does.  xcat
+ * store work is spread over all n tiles.  On row tiles the epilogue warps of
+ * each CTA copy their rows' share from the shards while the tile's main loop
+ * runs; on swapped tiles the MMA thread stores the landed boxes.  xcat
  * must not overlap the shards, Y, O or the workspace (AGMM_ERR_INVALID_ARG).
  * The workspace is agmm_workspace_bytes(plan, 0) bytes, as for agmm_run.
  */
