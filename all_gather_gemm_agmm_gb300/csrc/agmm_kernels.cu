@@ -403,7 +403,7 @@ __device__ __noinline__ void copy_x_rows(const KernelParams& p, const RingGeom& 
     }
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (dst[u] >= 0) *reinterpret_cast<uint4*>(xcat + dst[u]) = v[u];
+      if (dst[u] >= 0) __stcs(reinterpret_cast<uint4*>(xcat + dst[u]), v[u]);  // streaming: not re-read
   }
 }
 
