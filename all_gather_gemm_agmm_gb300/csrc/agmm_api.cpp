@@ -577,29 +577,35 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
   // Attributes and co-residency.  Swap path: the largest cluster (k split)
   // for which one wave of clusters covers every n tile; rows path: one
   // persistent CTA per SM.
+  const int swap_stages = pl->stages;  // the swapped tiles' depth before the reduction's buffers
   for (;;) {
     if (pl->key.path == kPathSwap) {
-      // The k-split reduction reuses the pipeline slots as its receive buffer:
-      // splits x cpo slots of 128 floats (cpo = owner columns, 16-aligned).
+      // k splits reduced through distributed shared memory: each rank's
+      // partial (Q quads of 128 x 4 floats, Q = the widest row group's slots
+      // / 4) is drained into its own pipeline memory, and a receive buffer of
+      // splits x ceil(Q / splits) quads follows the control block.  Fewer
+      // stages until both fit; if they cannot, the device-memory route (which
+      // needs neither buffer) with the same splits.
       const int64_t stage_bytes = (kASlotBytes + pl->b_slot_bytes) * pl->atoms;
-      const int64_t budget = (int64_t)kMaxDynSmem - 1024 - kCtlBytes;
-      const int64_t groups = (pl->group_chunks * (int64_t)pl->box_rows + 15) / 16;
-      const int64_t cpo = (groups + pl->splits - 1) / pl->splits * 16;
-      // With device-memory partials only the one-split local route uses it.
-      const bool via_smem = pl->splits == 1 || pl->swap_dsmem;
-      const int64_t recv = via_smem ? (int64_t)pl->splits * cpo * kTileM * 4 : 0;
-      while ((int64_t)pl->stages * stage_bytes < recv && (int64_t)(pl->stages + 1) * stage_bytes <= budget &&
-             pl->stages < kMaxStages)
-        ++pl->stages;
-      if ((int64_t)pl->stages * stage_bytes < recv) {
-        if (pl->splits <= 1) {
-          delete pl;
-          return fail(AGMM_ERR_UNSUPPORTED, "reduction buffer does not fit in shared memory");
+      const int64_t Q = (int64_t)pl->group_chunks * pl->box_rows / 4;
+      const int64_t quad = (int64_t)kTileM * 16;
+      const bool bulk = pl->splits > 1 && pl->swap_dsmem;
+      const int64_t recv = bulk ? pl->splits * ((Q + pl->splits - 1) / pl->splits) * quad : 0;
+      const int64_t avail = (int64_t)kMaxDynSmem - 1024 - kCtlBytes - recv;
+      if (bulk) {
+        int st = swap_stages;
+        while (st > 2 && (int64_t)st * stage_bytes > avail) --st;
+        if ((int64_t)st * stage_bytes > avail || (int64_t)st * stage_bytes < Q * quad) {
+          pl->swap_dsmem = false;
+          pl->stages = swap_stages;
+          continue;
         }
-        --pl->splits;
-        continue;
+        pl->stages = st;
+      } else {
+        pl->stages = swap_stages;
       }
-      pl->smem_bytes = tmem_safe_smem(1024 + (size_t)pl->stages * stage_bytes + kCtlBytes, pl->tmem_cols);
+      pl->smem_bytes =
+          tmem_safe_smem(1024 + (size_t)pl->stages * stage_bytes + kCtlBytes + (size_t)recv, pl->tmem_cols);
     }
     int active = 0;
     const int cluster = pl->key.path == kPathSwap ? pl->splits : pl->key.cm;
@@ -642,6 +648,7 @@ agmm_status_t plan_impl(int P, int64_t m_pd, int64_t k, int64_t n, agmm_dtype_t 
       const int64_t groups = (pl->group_chunks * (int64_t)pl->box_rows + 15) / 16;
       pl->tail_bytes = (size_t)pl->num_n_tiles * pl->row_groups * pl->splits * groups * 4 * kTileM * 16;
     }
+    if (pl->splits == 1) pl->swap_dsmem = false;
   } else {
     size_rows_grid(pl, pl->max_clusters);
   }

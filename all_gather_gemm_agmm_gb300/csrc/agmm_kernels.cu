@@ -71,7 +71,11 @@ __device__ __forceinline__ uint32_t bar_drain(uint32_t ctl) {
 // (1 arrival) and the contributors' "partial stored" (128 arrivals).
 __device__ __forceinline__ uint32_t bar_owner_go(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 5); }
 __device__ __forceinline__ uint32_t bar_published(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 6); }
-constexpr int kAbortOffset = 8 * (3 * kMaxStages + 7);  // int
+// Swapped tiles, k splits reduced through distributed shared memory: the
+// owner's receive barrier (1 arrival with the expected bytes, then the
+// other ranks' bulk copies).
+__device__ __forceinline__ uint32_t bar_recv(uint32_t ctl) { return ctl + 8u * (2 * kMaxStages + 7); }
+constexpr int kAbortOffset = 8 * (3 * kMaxStages + 8);  // int
 constexpr int kTmemOffset = kAbortOffset + 16;          // uint32
 constexpr int kChunkTabOffset = 512;                    // int4[kMaxSwapChunks]: shard, src_row, valid, out_row
 static_assert(kTmemOffset + 4 <= kChunkTabOffset, "control block overlap");
@@ -117,6 +121,20 @@ __device__ __forceinline__ int wait_phase(uint32_t bar, uint32_t parity, volatil
     }
     if (*abort) return kWaitAborted;
     if (ptx::clock_cycles() - t0 > limit_cycles) return kWaitTimeout;
+  }
+}
+
+// Bounded wait that polls with the non-blocking test: for barriers completed
+// by another CTA's bulk copies, where a blocked try_wait may wake late.
+__device__ __forceinline__ int wait_phase_poll(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_cycles) {
+  const uint64_t t0 = ptx::clock_cycles();
+  for (int i = 0;; ++i) {
+    if (ptx::mbar_test_wait(bar, parity)) return kWaitOk;
+    if ((i & 15) == 15) {
+      if (*abort) return kWaitAborted;
+      if (ptx::clock_cycles() - t0 > limit_cycles) return kWaitTimeout;
+    }
   }
 }
 
@@ -246,11 +264,6 @@ __device__ __forceinline__ uint32_t pack_16x2(float lo, float hi, bool f16) {
   return f16 ? hu : bu;
 }
 
-__device__ __forceinline__ uint16_t to_16(float v, bool f16) {
-  const uint16_t hu = __half_as_ushort(__float2half_rn(v));
-  const uint16_t bu = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  return f16 ? hu : bu;
-}
 
 // Store 32 consecutive f32 accumulator values of one output row.
 template <bool kF32>
@@ -272,25 +285,36 @@ __device__ __forceinline__ void store_row32(void* out, int64_t ldo, int64_t row,
   }
 }
 
-// Store one value.
+// Swapped tiles: writes output slots [s0, s0 + ns) of this CTA's row group
+// (gathered-row slots: chunk c0 + slot / box_rows, row slot % box_rows) for
+// the n tile's 128 columns, from float32 sums staged in shared memory as
+// stg[slot][128], rounded to the output type, as 16-byte stores along each
+// output row.  Threads t = 0..T-1 share the work.
 template <bool kF32>
-__device__ __forceinline__ void store_one(void* out, int64_t ldo, int64_t row, int64_t col, float v, bool f16) {
-  if constexpr (kF32) {
-    static_cast<float*>(out)[row * ldo + col] = v;
-  } else {
-    static_cast<uint16_t*>(out)[row * ldo + col] = to_16(v, f16);
-  }
-}
-
-// Store 4 consecutive values of one output row.
-template <bool kF32>
-__device__ __forceinline__ void store_row4(void* out, int64_t ldo, int64_t row, int64_t col,
-                                           float4 s, bool f16) {
-  if constexpr (kF32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(out) + row * ldo + col) = s;
-  } else {
-    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + row * ldo + col) =
-        make_uint2(pack_16x2(s.x, s.y, f16), pack_16x2(s.z, s.w, f16));
+__device__ __forceinline__ void store_slots(const KernelParams& p, const float* stg, int s0, int ns,
+                                            const int4* chunk_tab, int c0, int nt, int t, int T) {
+  constexpr int kPieces = kF32 ? kTileM / 4 : kTileM / 8;  // 16-byte pieces per 128-column row
+  for (int u = t; u < ns * kPieces; u += T) {
+    const int sl = u / kPieces;
+    const int pc = u - sl * kPieces;
+    const int cj = s0 + sl;
+    const int4 e = chunk_tab[c0 + (cj >> p.box_shift)];
+    const int r = cj & (p.box_rows - 1);
+    if (r >= e.z) continue;
+    const float* src = stg + (size_t)sl * kTileM;
+    const int64_t row = (int64_t)e.w + r;
+    const int64_t col = (int64_t)nt * kTileM;
+    if constexpr (kF32) {
+      const float4 v = *reinterpret_cast<const float4*>(src + pc * 4);
+      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * p.ldo + col + pc * 4) = v;
+    } else {
+      const float4 a = *reinterpret_cast<const float4*>(src + pc * 8);
+      const float4 b = *reinterpret_cast<const float4*>(src + pc * 8 + 4);
+      const bool f16 = p.f16 != 0;
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.ldo + col + pc * 8) =
+          make_uint4(pack_16x2(a.x, a.y, f16), pack_16x2(a.z, a.w, f16), pack_16x2(b.x, b.y, f16),
+                     pack_16x2(b.z, b.w, f16));
+    }
   }
 }
 
@@ -302,16 +326,14 @@ struct OwnerSlice {
   size_t slot_quads;    // quads per rank's slot
   int q0;               // first quad owned
   int items;            // owned (quad, column) pairs
-  const int4* chunk_tab;
-  int c0;               // first chunk of the row group
-  int nt;               // n tile
 };
 
 // The (quad, column) items are spread over all warps.  Each thread issues
 // every rank's 16-byte load for kH items before summing (kH x kS loads in
-// flight, at most 24), then adds them in rank order.
-template <bool kF32, int kS>
-__device__ __forceinline__ void owner_sum_global(const KernelParams& p, const OwnerSlice& os) {
+// flight, at most 24), then adds them in rank order and stages the sums in
+// shared memory, stg[slot - 4 * q0][128] (written out by store_slots).
+template <int kS>
+__device__ __forceinline__ void owner_sum_global(const OwnerSlice& os, float* stg) {
   constexpr int kH = (24 / kS) < 1 ? 1 : ((24 / kS) > 4 ? 4 : (24 / kS));
 #pragma unroll 1
   for (int i = threadIdx.x; i < os.items; i += kH * kThreads) {
@@ -340,17 +362,44 @@ __device__ __forceinline__ void owner_sum_global(const KernelParams& p, const Ow
           sum.z += part[h][rk].z;
           sum.w += part[h][rk].w;
         }
-        const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
-        const int64_t ncol = (int64_t)os.nt * kTileM + t;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int cj = q * 4 + j;
-          const int4 e = os.chunk_tab[os.c0 + (cj >> p.box_shift)];
-          const int r = cj & (p.box_rows - 1);
-          if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j], p.f16 != 0);
-        }
+        float* dst = stg + (size_t)(q - os.q0) * 4 * kTileM + t;
+        dst[0] = sum.x;
+        dst[kTileM] = sum.y;
+        dst[2 * kTileM] = sum.z;
+        dst[3 * kTileM] = sum.w;
       }
     }
+  }
+}
+
+// Swap path, shared-memory mode: the owner's sum of its quads [q0, q0 +
+// items/128) over the kS ranks, in rank order, from its own partial (rank
+// `split`, send[quad][lane]) and the copies the others sent
+// (recv[rank][quad - q0][lane], qmax quads per rank); staged like
+// owner_sum_global.  All threads of the CTA share the (quad, lane) items.
+template <int kS>
+__device__ __forceinline__ void owner_sum_smem(const float4* send, const float4* recv, int qmax, int split, int q0,
+                                               int items, float* stg) {
+  for (int it = threadIdx.x; it < items; it += kThreads) {
+    const int q = q0 + (it >> 7);
+    const int t = it & (kTileM - 1);
+    float4 part[kS];
+#pragma unroll
+    for (int rk = 0; rk < kS; ++rk)
+      part[rk] = rk == split ? send[q * kTileM + t] : recv[(rk * qmax + (q - q0)) * kTileM + t];
+    float4 sum = part[0];
+#pragma unroll
+    for (int rk = 1; rk < kS; ++rk) {
+      sum.x += part[rk].x;
+      sum.y += part[rk].y;
+      sum.z += part[rk].z;
+      sum.w += part[rk].w;
+    }
+    float* dst = stg + (q - q0) * 4 * kTileM + t;
+    dst[0] = sum.x;
+    dst[kTileM] = sum.y;
+    dst[2 * kTileM] = sum.z;
+    dst[3 * kTileM] = sum.w;
   }
 }
 
@@ -467,8 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     ptx::mbar_init(bar_drain(ctl), 1);
     ptx::mbar_init(bar_owner_go(ctl), 1);
     ptx::mbar_init(bar_published(ctl), 128);
+    ptx::mbar_init(bar_recv(ctl), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
+    if (kPath == kPathSwap && p.splits > 1 && p.swap_partials == nullptr) {
+      // this owner's quads of each other rank's partial (see the reduction)
+      const int gc = min(p.group_chunks, p.total_chunks - (int)blockIdx.z * p.group_chunks);
+      const int Q = gc * p.box_rows / 4;
+      const int mine = (int)(((int64_t)(blockIdx.x + 1) * Q) / p.splits) - (int)(((int64_t)blockIdx.x * Q) / p.splits);
+      ptx::mbar_arrive_expect_tx(bar_recv(ctl), (uint32_t)((p.splits - 1) * mine) * (uint32_t)kTileM * 16u);
+    }
   }
   if (warp == 0 && lane == 0) {
     for (int r = 0; r < p.P; ++r) ptx::prefetch_tensormap(&p.xmap[r]);
@@ -499,6 +556,11 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     ptx::cluster_arrive_relaxed();
     ptx::cluster_wait();
   }
+  // Swapped tiles reducing their k splits through distributed shared memory:
+  // the other ranks copy into this CTA's receive buffer and signal its
+  // receive barrier; the matching wait comes before the first such copy.
+  const bool swap_bulk = kPath == kPathSwap && p.splits > 1 && p.swap_partials == nullptr;
+  if (swap_bulk) ptx::cluster_arrive_relaxed();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Everything above touched only shared memory, tensor memory and the
@@ -1043,110 +1105,97 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
     // Reduction of the k splits of this CTA's (n tile, row group).  The
     // accumulator holds 128 n columns (TMEM lanes) x ncols gathered-row slots
     // (TMEM columns): chunks c0.. of the ring-ordered chunk table, box_rows
-    // slots each.  With one split the CTA is its own owner.
+    // slots each.  A quad is 4 slots of all 128 lanes ([lane][4 floats], 2
+    // KiB); owner o (rank o of the cluster) sums quads [o*Q/S, (o+1)*Q/S) of
+    // every rank's partial in rank order, so every output element has one
+    // fixed reduction order whatever the route.
+    //   one split:      the CTA stores its accumulator directly;
+    //   device memory:  each rank stores its partial to its own slot in an
+    //                   L2-resident workspace with coalesced 16-byte stores;
+    //                   a cluster barrier (release/acquire) orders them
+    //                   before the owners' loads;
+    //   shared memory:  each rank drains its partial into its own pipeline
+    //                   memory (idle after its main loop), then bulk-copies
+    //                   owner o's quads into slot [rank] of owner o's receive
+    //                   buffer (past the control block), counted on o's
+    //                   receive barrier; owners wait only for their bytes, so
+    //                   early ranks' copies land while late ranks still work.
     const int ncols = swap_nch * p.box_rows;
     const int S = p.splits;
     const int groups = (ncols + 15) >> 4;
+    const int Q = ncols >> 2;
+    const int q_lo = (int)(((int64_t)split * Q) / S);
+    const int q_hi = (int)(((int64_t)(split + 1) * Q) / S);
     // Slot size of the device-memory mode: the widest row group's columns.
     const int slot_groups = (p.group_chunks * p.box_rows + 15) >> 4;
     const size_t slot_quads = (size_t)slot_groups * 4;
-    // Device-memory mode: each rank stores its partial to its own slot
-    // [quad][128 lanes][4 floats] in an L2-resident workspace with coalesced
-    // 16-byte stores; barrier 2 (release/acquire at cluster scope) orders them
-    // before the owners' loads.  Owner o sums quads [o*Q/S, (o+1)*Q/S) over
-    // every rank, in rank order.
-    // Shared-memory mode: owner o holds 16-slot groups [o*cpo, (o+1)*cpo) and
-    // recv[r][lq][lane][4] in its shared memory receives rank r's partial of
-    // slots 4*lq..4*lq+3; ranks push with 16-byte remote stores once every
-    // CTA's pipeline memory is idle (barrier 1).
     const bool global_mode = S > 1 && p.swap_partials != nullptr;
-    const int cpo = ((groups + S - 1) / S) * 16;
-    const uint32_t quad_bytes = (uint32_t)kTileM * 16u;  // one [lane][4] block
+    constexpr uint32_t kQuadBytes = (uint32_t)kTileM * 16u;
     float4* gslot = global_mode ? reinterpret_cast<float4*>(p.swap_partials) +
                                       ((size_t)swap_cl * S) * slot_quads * kTileM
                                 : nullptr;
+    const int tl = (warp & 3) * 32 + lane;  // epilogue thread: TMEM lane = n column
     __syncwarp();
-    if (S > 1 && !global_mode) ptx::cluster_sync_all();  // 1: all CTAs have drained their main loop
     trace(p, 8);
-    if (warp >= 2 && global_mode) {
-      const int tl = (warp & 3) * 32 + lane;
-      float4* mine = gslot + (size_t)split * slot_quads * kTileM + tl;
-      const uint32_t tbase = lane_base_of(tmem_base, warp);
+    // staged sums, [slot][128 columns] float32 (pipeline memory, idle now)
+    float* const stg = reinterpret_cast<float*>(base_ptr);
+    if (S == 1) {
+      if (warp >= 2) {
+        if (!*abort_flag) {
+          const uint32_t tbase = lane_base_of(tmem_base, warp);
 #pragma unroll 1
-      for (int g = 0; g < groups; g += 2) {
-        uint32_t v[2][16];
-        ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 16), v[0]);
-        if (g + 1 < groups) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)((g + 1) * 16), v[1]);
-        ptx::tmem_ld_wait();
+          for (int g = 0; g < groups; ++g) {
+            uint32_t v[16];
+            ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 16), v);
+            ptx::tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (g + h < groups) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              mine[((size_t)(g + h) * 4 + q4) * kTileM] =
-                  make_float4(__uint_as_float(v[h][4 * q4]), __uint_as_float(v[h][4 * q4 + 1]),
-                              __uint_as_float(v[h][4 * q4 + 2]), __uint_as_float(v[h][4 * q4 + 3]));
+            for (int i = 0; i < 16; ++i)
+              if (g * 16 + i < ncols) stg[(size_t)(g * 16 + i) * kTileM + tl] = __uint_as_float(v[i]);
           }
+          ptx::tc_fence_before();
         }
+        // the four epilogue warps' slots staged (every thread arrives, also
+        // on an abort, so the bounded wait below cannot be stranded)
+        ptx::mbar_arrive(bar_published(ctl));
+        int res = kWaitOk;
+        if (lane == 0) res = wait_phase(bar_published(ctl), 0, abort_flag, limit);
+        res = __shfl_sync(0xffffffffu, res, 0);
+        if (res == kWaitOk && !*abort_flag)
+          store_slots<kF32>(p, stg, 0, ncols, chunk_tab, swap_c0, swap_nt, tl, kTileM);
       }
-      ptx::tc_fence_before();
-    } else if (warp >= 2) {
-      const uint32_t lane_off = (uint32_t)(((warp & 3) * 32 + lane) * 16);
-      const uint32_t my_slot0 = base + (uint32_t)(split * (cpo >> 2)) * quad_bytes + lane_off;
-      const uint32_t tbase = lane_base_of(tmem_base, warp);
-      // Two 16-column groups per round: both TMEM loads in flight, then
-      // straight-line stores (each group belongs to a single owner).  Each
-      // rank starts at its own owner's groups, so the ranks of a cluster write
-      // to different owners at any moment instead of all to the same one.
-      const int gpo = cpo >> 4;  // groups per owner
-      const int g_start = (split * gpo) % groups;
+    } else if (global_mode) {
+      if (warp >= 2) {
+        float4* mine = gslot + (size_t)split * slot_quads * kTileM + tl;
+        const uint32_t tbase = lane_base_of(tmem_base, warp);
 #pragma unroll 1
-      for (int gi = 0; gi < groups; gi += 2) {
-        uint32_t v[2][16];
-        int gsel[2];
-        gsel[0] = g_start + gi;
-        if (gsel[0] >= groups) gsel[0] -= groups;
-        gsel[1] = gsel[0] + 1;
-        if (gsel[1] >= groups) gsel[1] -= groups;
-        ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(gsel[0] * 16), v[0]);
-        if (gi + 1 < groups) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(gsel[1] * 16), v[1]);
-        ptx::tmem_ld_wait();
+        for (int g = 0; g < groups; g += 2) {
+          uint32_t v[2][16];
+          ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 16), v[0]);
+          if (g + 1 < groups) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)((g + 1) * 16), v[1]);
+          ptx::tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (gi + h < groups) {
-            const int col0 = gsel[h] * 16;
-            const int o = col0 / cpo;
-            const uint32_t la = my_slot0 + (uint32_t)((col0 - o * cpo) >> 2) * quad_bytes;
-            if (S > 1) {
-              const uint32_t ra = ptx::map_shared_rank(la, (uint32_t)o);
+          for (int h = 0; h < 2; ++h) {
+            if (g + h < groups) {
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4)
-                ptx::st_shared_cluster_v4(ra + q4 * quad_bytes, v[h][4 * q4], v[h][4 * q4 + 1], v[h][4 * q4 + 2],
-                                          v[h][4 * q4 + 3]);
-            } else {
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                ptx::st_shared_v4(la + q4 * quad_bytes, v[h][4 * q4], v[h][4 * q4 + 1], v[h][4 * q4 + 2],
-                                  v[h][4 * q4 + 3]);
+                mine[((size_t)(g + h) * 4 + q4) * kTileM] =
+                    make_float4(__uint_as_float(v[h][4 * q4]), __uint_as_float(v[h][4 * q4 + 1]),
+                                __uint_as_float(v[h][4 * q4 + 2]), __uint_as_float(v[h][4 * q4 + 3]));
             }
           }
         }
+        ptx::tc_fence_before();
       }
-      ptx::tc_fence_before();
-    }
-    __syncwarp();
-    if (S > 1) ptx::cluster_sync_all(); else __syncthreads();  // 2: partials delivered
-    trace(p, 9);
-    if (global_mode) {
-      if (!*abort_flag) {
-        const int Q = ncols >> 2;
-        const int q0 = (int)(((int64_t)split * Q) / S);
-        const int q1 = (int)(((int64_t)(split + 1) * Q) / S);
-        const OwnerSlice os{gslot, slot_quads, q0, (q1 - q0) * kTileM, chunk_tab, swap_c0, swap_nt};
+      __syncwarp();
+      ptx::cluster_sync_all();  // partials delivered
+      trace(p, 9);
+      // one decision for the whole CTA, so the barrier below is reached by all
+      if (__syncthreads_or(*abort_flag) == 0) {
+        const OwnerSlice os{gslot, slot_quads, q_lo, (q_hi - q_lo) * kTileM};
         switch (S) {
 #define AGMM_OWNER_CASE(N) \
   case N:                  \
-    owner_sum_global<kF32, N>(p, os); \
+    owner_sum_global<N>(os, stg); \
     break;
           AGMM_OWNER_CASE(2) AGMM_OWNER_CASE(3) AGMM_OWNER_CASE(4) AGMM_OWNER_CASE(5) AGMM_OWNER_CASE(6)
           AGMM_OWNER_CASE(7) AGMM_OWNER_CASE(8) AGMM_OWNER_CASE(9) AGMM_OWNER_CASE(10) AGMM_OWNER_CASE(11)
@@ -1155,43 +1204,100 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
           default:
             break;
         }
+        __syncthreads();
+        store_slots<kF32>(p, stg, q_lo * 4, (q_hi - q_lo) * 4, chunk_tab, swap_c0, swap_nt, threadIdx.x, kThreads);
       }
-    } else if (warp >= 2 && !*abort_flag) {
-      // Thread t sums lane t (n column swap_nt*128 + t) of four slots at a time.
-      const int t = threadIdx.x - 64;
-      const int c0 = split * cpo;
-      const int c1 = min(ncols, c0 + cpo);
-      const float4* recv = reinterpret_cast<const float4*>(base_ptr);
-      const int qpo = cpo >> 2;  // quads per owner slot range
-      const int64_t ncol = (int64_t)swap_nt * kTileM + t;
-      for (int c = c0; c < c1; c += 4) {
-        const int lq = (c - c0) >> 2;
-        // Issue every rank's load first (independent), then add in rank order.
-        float4 part[kMaxSplits];
+    } else {
+      // shared-memory mode: send buffer [quad][lane][16 B] at the start of
+      // the pipeline memory, receive buffer [rank][qmax quads][lane][16 B]
+      // past the control block
+      const int qmax = (Q + S - 1) / S;
+      const uint32_t send = base;
+      const uint32_t recv = ctl + (uint32_t)kCtlBytes;
+      if (warp >= 2) {
+        if (!*abort_flag) {
+          const uint32_t tbase = lane_base_of(tmem_base, warp);
+          const uint32_t lane_off = (uint32_t)tl * 16u;
+#pragma unroll 1
+          for (int g = 0; g < groups; g += 2) {
+            uint32_t v[2][16];
+            ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 16), v[0]);
+            if (g + 1 < groups) ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)((g + 1) * 16), v[1]);
+            ptx::tmem_ld_wait();
 #pragma unroll
-        for (int rk = 0; rk < kMaxSplits; ++rk)
-          if (rk < S) part[rk] = recv[((size_t)(rk * qpo + lq)) * kTileM + t];
-        float4 sum = part[0];
+            for (int h = 0; h < 2; ++h) {
 #pragma unroll
-        for (int rk = 1; rk < kMaxSplits; ++rk) {
-          if (rk < S) {
-            sum.x += part[rk].x;
-            sum.y += part[rk].y;
-            sum.z += part[rk].z;
-            sum.w += part[rk].w;
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const int q = (g + h) * 4 + q4;
+                if (g + h < groups && q < Q)
+                  ptx::st_shared_v4(send + (uint32_t)q * kQuadBytes + lane_off, v[h][4 * q4], v[h][4 * q4 + 1],
+                                    v[h][4 * q4 + 2], v[h][4 * q4 + 3]);
+              }
+            }
+          }
+          ptx::tc_fence_before();
+        }
+        // the bulk copies read what the generic stores wrote
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bar_published(ctl));
+      }
+      __syncwarp();
+      // every owner has initialised its receive barrier
+      ptx::cluster_wait();
+      trace(p, 9);
+      if (warp == 2) {
+        int res = kWaitOk;
+        if (lane == 0) res = wait_phase_poll(bar_published(ctl), 0, abort_flag, limit);
+        res = __shfl_sync(0xffffffffu, res, 0);
+        if (res != kWaitOk) {
+          if (lane == 0) record_failure(p, abort_flag, res, kRoleEpilogue, -5, swap_nt);
+        } else if (!*abort_flag && ptx::elect_one()) {
+          for (int o = 0; o < S; ++o) {
+            const int lo = (int)(((int64_t)o * Q) / S);
+            const int hi = (int)(((int64_t)(o + 1) * Q) / S);
+            if (o == split || hi <= lo) continue;
+            ptx::bulk_copy_to_cluster(ptx::map_shared_rank(recv + (uint32_t)(split * qmax) * kQuadBytes, (uint32_t)o),
+                                      send + (uint32_t)lo * kQuadBytes, (uint32_t)(hi - lo) * kQuadBytes,
+                                      ptx::map_shared_rank(bar_recv(ctl), (uint32_t)o));
           }
         }
-        const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int cj = c + j;
-          if (cj < c1) {
-            const int4 e = chunk_tab[swap_c0 + (cj >> p.box_shift)];
-            const int r = cj & (p.box_rows - 1);
-            if (r < e.z) store_one<kF32>(p.out, p.ldo, (int64_t)e.w + r, ncol, vals[j], p.f16 != 0);
+        __syncwarp();
+      }
+      {
+        // every warp waits for this owner's bytes, then all threads sum
+        int res = kWaitOk;
+        if (lane == 0) res = wait_phase_poll(bar_recv(ctl), 0, abort_flag, limit);
+        res = __shfl_sync(0xffffffffu, res, 0);
+        if (res != kWaitOk && lane == 0) record_failure(p, abort_flag, res, kRoleEpilogue, -6, swap_nt);
+        // one decision for the whole CTA, so the barrier below is reached by all
+        if (__syncthreads_or(*abort_flag) == 0) {
+          // sums staged in this CTA's own (unused) receive slot, [slot][128]
+          const float4* const sendv = reinterpret_cast<const float4*>(base_ptr);
+          const float4* const recvv = reinterpret_cast<const float4*>(base_ptr + (recv - base));
+          float* const own = reinterpret_cast<float*>(base_ptr + (recv - base)) + (size_t)split * qmax * 4 * kTileM;
+          const int items = (q_hi - q_lo) * kTileM;
+          switch (S) {
+#define AGMM_OWNER_CASE(N) \
+  case N:                  \
+    owner_sum_smem<N>(sendv, recvv, qmax, split, q_lo, items, own); \
+    break;
+            AGMM_OWNER_CASE(2) AGMM_OWNER_CASE(3) AGMM_OWNER_CASE(4) AGMM_OWNER_CASE(5) AGMM_OWNER_CASE(6)
+            AGMM_OWNER_CASE(7) AGMM_OWNER_CASE(8) AGMM_OWNER_CASE(9) AGMM_OWNER_CASE(10) AGMM_OWNER_CASE(11)
+            AGMM_OWNER_CASE(12) AGMM_OWNER_CASE(13) AGMM_OWNER_CASE(14) AGMM_OWNER_CASE(15) AGMM_OWNER_CASE(16)
+#undef AGMM_OWNER_CASE
+            default:
+              break;
           }
+          __syncthreads();
+          store_slots<kF32>(p, own, q_lo * 4, (q_hi - q_lo) * 4, chunk_tab, swap_c0, swap_nt, threadIdx.x, kThreads);
         }
       }
+      __syncwarp();
+      // No CTA leaves while copies out of or into its shared memory may run:
+      // each arrives once its own bytes are in (relaxed: it publishes no
+      // memory through this barrier).
+      ptx::cluster_arrive_relaxed();
+      ptx::cluster_wait();
     }
     trace(p, 10);
   }

@@ -190,6 +190,7 @@ def test_swap_row_groups(agmm, case, monkeypatch):
     monkeypatch.setenv("AGMM_PATH", "1")
     monkeypatch.setenv("AGMM_SPLITK", "4")
     outs = {}
+    used_dsmem = 0
     for dsmem in ("0", "1"):
         monkeypatch.setenv("AGMM_SWAP_DSMEM", dsmem)
         for groups in ("1", "2", "4"):
@@ -200,7 +201,10 @@ def test_swap_row_groups(agmm, case, monkeypatch):
             if info["row_groups"] != int(groups):
                 continue  # that many groups would leave one empty
             check(o, ref32, f"groups={groups} dsmem={dsmem} {info}")
+            assert info["splits"] == 4, info  # both routes keep the k splits
             outs[(dsmem, groups)] = o
+            used_dsmem += info["dsmem_reduce"]
     base = outs[("0", "1")]
     for key, o in outs.items():
         assert torch.equal(base.view(torch.int16), o.view(torch.int16)), key
+    assert used_dsmem > 0  # the distributed-shared-memory route ran
