@@ -19,9 +19,11 @@ Pins:
   * shard permutation permutes the output row blocks.
   * scaling Y by 2 scales O by exactly 2.
   * brute force with exact rationals on tiny shapes, then exact RNE to bf16.
+  * bf16 decoding: all 65536 patterns against the binary32 upper-half rule.
 """
 from __future__ import annotations
 
+import ctypes
 import json
 import os
 from fractions import Fraction
@@ -406,7 +408,21 @@ def pin_f16_bruteforce_exact(lib):
                     assert int(o16[i, j]) == want, (trial, i, j, hex(int(o16[i, j])), hex(want))
 
 
-ALL_PINS = [pin_bf16_golden, pin_bf16_vs_torch, pin_hand_example, pin_plain_matmul_p1,
+def pin_bf16_decode_all_patterns(lib):
+    # bf16 is the upper half of a binary32 pattern: every one of the 65536
+    # patterns decodes, through both of the oracle's decoders, to that
+    # binary32 value (compared bit for bit, so NaN payloads count too)
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    want = (bits.astype(np.uint32) << 16).view(np.float32)
+    got = np.empty(65536, dtype=np.float32)
+    lib.oracle_bf16_array_to_f32(bits.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
+                                 got.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), 65536)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    for b in (0x0000, 0x8000, 0x3F80, 0xBF80, 0x7F80, 0xFF80, 0x0001, 0x7FC0):
+        assert np.float32(lib.oracle_bf16_to_f32(b)).view(np.uint32) == np.uint32(b) << np.uint32(16)
+
+
+ALL_PINS = [pin_bf16_golden, pin_bf16_decode_all_patterns, pin_bf16_vs_torch, pin_hand_example, pin_plain_matmul_p1,
             pin_identity_embedding, pin_shard_isolation, pin_shard_permutation, pin_scale_by_two,
             pin_bruteforce_exact, pin_layout_consistency, pin_double_mode_close, pin_row_range,
             pin_f16_golden, pin_f16_vs_torch, pin_f16_plain_matmul_p1, pin_f16_identity_embedding,
@@ -465,6 +481,8 @@ MUTANTS = {
     "f16_subnormal_scale": ("const int shift = e >= 1 ? 13 : 14 - e;", "const int shift = e >= 1 ? 13 : 13 - e;"),
     "f16_no_overflow": ("if (e >= 31) return (uint16_t)(sign | 0x7C00u);", "if (e >= 32) return (uint16_t)(sign | 0x7C00u);"),
     "f16_decode_bias": ("((uint32_t)(e - 15 + 127) << 23)", "((uint32_t)(e - 16 + 127) << 23)"),
+    # the bf16 decoder
+    "bf16_decode_shift": ("uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)b) << 15;"),
 }
 
 
