@@ -208,3 +208,39 @@ def test_swap_row_groups(agmm, case, monkeypatch):
     for key, o in outs.items():
         assert torch.equal(base.view(torch.int16), o.view(torch.int16)), key
     assert used_dsmem > 0  # the distributed-shared-memory route ran
+
+
+@pytest.mark.parametrize("case", [(4, 64, 1024, 512, True), (3, 13, 768, 384, False), (8, 8, 2048, 256, True)],
+                         ids=lambda c: "P{}_m{}_k{}".format(c[0], c[1], c[2]))
+def test_swap_reduction_routes(agmm, case):
+    # Swapped tiles reduce their k splits one of three ways: no split (the
+    # CTA stores its own accumulator), through an L2-resident workspace, or
+    # by bulk copies into the owners' shared memory.  Every route meets the
+    # oracle in bf16 and float32 output; with the same splits the two
+    # cross-CTA routes agree bitwise (same rank-order sums).
+    P, m, k, n, rt = case
+    xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=21)
+    ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+    for splits in (1, 5, 8, 16):
+        outs = {}
+        for dsmem in (False, True):
+            cfg = {"path": "swap", "splits": splits, "dsmem_reduce": dsmem, "tuned_table": False}
+            try:
+                plan = agmm.Plan(P, m, k, n, rt, config=cfg)
+            except agmm.AgmmError as e:
+                assert e.status == agmm.AGMM_ERR_UNSUPPORTED, e
+                continue
+            info = plan.info()
+            assert info["path"] == 1
+            for f32 in (False, True):
+                pl = plan if not f32 else agmm.Plan(P, m, k, n, rt, out_f32=True, config=cfg)
+                o, _ = _run(agmm, xs_cpu, y_cpu, rt, my_id=P - 1, f32=f32, plan=pl)
+                check(o, ref32, f"splits={splits} dsmem={dsmem} f32={f32} {pl.info()}")
+                if not f32:
+                    outs[(dsmem, info["splits"], info["dsmem_reduce"])] = o
+        same_split = {}
+        for (dsmem, s, used), o in outs.items():
+            same_split.setdefault(s, []).append(o)
+        for s, os_ in same_split.items():
+            for o in os_[1:]:
+                assert torch.equal(os_[0].view(torch.int16), o.view(torch.int16)), (case, s)
