@@ -93,6 +93,24 @@ def reduce_sum(value: float, device=None) -> float:
     return float(t.item())
 
 
+def uniform_count(n: int, device=None) -> int:
+    """The largest of the ranks' counts, on every rank: every rank must time
+    the same number of barrier-bracketed batches and capture the same K."""
+    return int(round(reduce_max(float(n), device)))
+
+
+def batches_for(est_step_s: float, K: int, min_batches: int = 7, min_timed_s: float = 0.5,
+                max_batches: int = 400) -> int:
+    """Batches of K steps to time: at least min_batches and about min_timed_s
+    of timed work, at most max_batches."""
+    return int(min(max_batches, max(min_batches, -(-min_timed_s // max(est_step_s * K, 1e-7)))))
+
+
+def steps_for(est_step_s: float, K_min: int, batch_s: float = 2e-3, K_max: int = 2000) -> int:
+    """Steps per batch for a sub-result: at least K_min and about batch_s of work."""
+    return int(max(K_min, min(K_max, -(-batch_s // max(est_step_s, 1e-9)))))
+
+
 def aggregate_throughput(units_this_rank: float, seconds_this_rank: float, device=None):
     """Whole-job throughput: all ranks' units over the slowest rank's time."""
     total = reduce_sum(units_this_rank, device)
@@ -296,7 +314,7 @@ def measure(step_fns, K, warmup, stream, device, min_batches=7, min_timed_s=0.5,
 
     est = estimate_step_s(step_fns, stream)
     graph = capture_steps(step_fns, K, warmup, stream)
-    B = int(min(max_batches, max(min_batches, -(-min_timed_s // max(est * K, 1e-7)))))
+    B = uniform_count(batches_for(est, K, min_batches, min_timed_s, max_batches), device)
     times, clocks = time_batches(graph, stream, B, sampler)
     del graph
     med = st.median(times)
@@ -419,7 +437,7 @@ def sub_result(args, name, device, stream, peaks, peak_src):
     wb = WorkloadBench(w, device, args.dtype)
     fused = wb.fused()
     est = estimate_step_s(fused, stream)
-    K = int(max(args.steps or 20, min(2000, -(-2e-3 // est))))
+    K = uniform_count(steps_for(est, args.steps or 20), device)
     f, _ = measure(fused, K, args.warmup, stream, device)
     wb.plan.query_status(wb.ws, stream)
     u, _ = measure(wb.unfused(), K, args.warmup, stream, device)
@@ -584,7 +602,7 @@ def bench_sweep(args):
         wb = WorkloadBench(w, device, args.dtype)
         fused = wb.fused()
         est = estimate_step_s(fused, stream)
-        K = int(max(args.steps or 20, min(2000, -(-2e-3 // est))))
+        K = steps_for(est, args.steps or 20)
         f, _ = measure(fused, K, args.warmup, stream, device)
         wb.plan.query_status(wb.ws, stream)
         u, _ = measure(wb.unfused(), K, args.warmup, stream, device)
