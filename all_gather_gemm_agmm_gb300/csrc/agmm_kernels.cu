@@ -501,35 +501,44 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
   // The next kernel in the stream may start its prologue on free SMs; it waits
   // (griddepcontrol.wait) for this grid to finish before touching memory.
   if (threadIdx.x == 0) ptx::griddep_launch_dependents();
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+  if (warp == 0) {
+    // The lanes of warp 0 initialise one barrier each (lane L: full[L] for L
+    // < S, empty[L - S], then the accumulator, drain and hand-off barriers)
+    // and each fences its own initialisation; the tensor maps are prefetched
+    // by lane as well.
+    const int b = lane;
+    if (b < S) {
       // a pair: both producers count their bytes on the leader's barrier
-      ptx::mbar_init(bar_full(ctl, s), kPair ? 2 : 1);
+      ptx::mbar_init(bar_full(ctl, b), kPair ? 2 : 1);
+    } else if (b < 2 * S) {
       // the MMA frees the stage (a pair: the leader's MMA, for both CTAs)
-      ptx::mbar_init(bar_empty(ctl, s), 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(bar_acc_full(ctl, a), 1);
+      ptx::mbar_init(bar_empty(ctl, b - S), 1);
+    } else if (b < 2 * S + 2) {
+      ptx::mbar_init(bar_acc_full(ctl, b - 2 * S), 1);
+    } else if (b < 2 * S + 4) {
       // a pair: both CTAs' epilogues drain the accumulator the leader fills
-      ptx::mbar_init(bar_acc_empty(ctl, a), kPair ? 256 : 128);
+      ptx::mbar_init(bar_acc_empty(ctl, b - 2 * S - 2), kPair ? 256 : 128);
+    } else if (b == 2 * S + 4) {
+      ptx::mbar_init(bar_drain(ctl), 1);
+    } else if (b == 2 * S + 5) {
+      ptx::mbar_init(bar_owner_go(ctl), 1);
+    } else if (b == 2 * S + 6) {
+      ptx::mbar_init(bar_published(ctl), 128);
+    } else if (b == 2 * S + 7) {
+      ptx::mbar_init(bar_recv(ctl), 1);
     }
-    ptx::mbar_init(bar_drain(ctl), 1);
-    ptx::mbar_init(bar_owner_go(ctl), 1);
-    ptx::mbar_init(bar_published(ctl), 128);
-    ptx::mbar_init(bar_recv(ctl), 1);
-    *abort_flag = 0;
+    if (lane < p.P) ptx::prefetch_tensormap(&p.xmap[lane]);
+    if (lane == 31) ptx::prefetch_tensormap(&p.ymap);
+    if (lane == 0) *abort_flag = 0;
     ptx::fence_mbar_init();
-    if (kPath == kPathSwap && p.splits > 1 && p.swap_partials == nullptr) {
+    __syncwarp();
+    if (lane == 0 && kPath == kPathSwap && p.splits > 1 && p.swap_partials == nullptr) {
       // this owner's quads of each other rank's partial (see the reduction)
       const int gc = min(p.group_chunks, p.total_chunks - (int)blockIdx.z * p.group_chunks);
       const int Q = gc * p.box_rows / 4;
       const int mine = (int)(((int64_t)(blockIdx.x + 1) * Q) / p.splits) - (int)(((int64_t)blockIdx.x * Q) / p.splits);
       ptx::mbar_arrive_expect_tx(bar_recv(ctl), (uint32_t)((p.splits - 1) * mine) * (uint32_t)kTileM * 16u);
     }
-  }
-  if (warp == 0 && lane == 0) {
-    for (int r = 0; r < p.P; ++r) ptx::prefetch_tensormap(&p.xmap[r]);
-    ptx::prefetch_tensormap(&p.ymap);
   }
   if constexpr (kPath == kPathSwap) {
     // The ring-ordered chunk table, computed once per CTA (each row group of
@@ -606,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       uint64_t* wait_acc = p.trace ? &waited_empty : nullptr;
       const int cpt = kTileM / p.box_rows;
       SegmentIter iter;
-      iter.init(p, cluster_id, nclusters);
+      if constexpr (kPath == kPathRows) iter.init(p, cluster_id, nclusters);
       bool swap_pending = true;
       for (int tile = 0; ok; ++tile) {
         int mt = 0, nt = swap_nt;
@@ -798,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       uint64_t* wf = p.trace ? &waited_full : nullptr;
       uint64_t* wa = p.trace ? &waited_accfree : nullptr;
       SegmentIter iter;
-      iter.init(p, cluster_id, nclusters);
+      if constexpr (kPath == kPathRows) iter.init(p, cluster_id, nclusters);
       const uint32_t chunk_bytes = (uint32_t)p.box_rows * 128u;
       bool stored_any = false;
       for (int tile = 0; ok; ++tile, ++it) {
