@@ -1,6 +1,7 @@
 """Build the sm_103a shared library ``libagmm.so`` in-tree with nvcc.
 
-Two translation units (kernels, C ABI) compile in parallel to objects under
+The translation units (kernel variants in three groups, selection and launch,
+C ABI, allocation-free entry point) compile in parallel to objects under
 ``_build/`` and link, with the CUDA runtime linked statically, into
 ``all_gather_gemm_agmm_gb300/libagmm.so``.  No cmake, one ``-gencode``.
 """
@@ -18,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libagmm.so")
-SOURCES = ["agmm_kernels.cu", "agmm_api.cpp", "agmm_noalloc.cu"]
+SOURCES = ["agmm_select_rows_a1.cu", "agmm_select_rows_a2.cu", "agmm_select_swap.cu", "agmm_kernels.cu",
+           "agmm_api.cpp", "agmm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

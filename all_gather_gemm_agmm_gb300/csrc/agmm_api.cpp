@@ -134,7 +134,7 @@ struct agmm_plan_s {
   int box_rows = 0, total_chunks = 0, num_m_tiles = 0, num_mc_tiles = 0, num_n_tiles = 0, num_k_blocks = 0;
   int group_m = 1, num_tiles = 0, stages = 0, mma_n = 0, tmem_cols = 0, splits = 1;
   uint32_t b_slot_bytes = 0;
-  int atoms = 1;  // k blocks per pipeline stage (swapped tiles: 1 or 2)
+  int atoms = 1;  // k blocks per pipeline stage (1 or 2)
   size_t smem_bytes = 0;
   dim3 grid{1, 1, 1};
   int cluster_x = 1;
@@ -487,7 +487,18 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
     pl->num_tiles = pl->num_mc_tiles * pl->num_n_tiles;
     pl->mma_n = bn;
     pl->b_slot_bytes = (uint32_t)(pl->key.pair ? bn / 2 : bn) * 128u;
-    const int64_t stage_bytes = kASlotBytes + pl->b_slot_bytes;
+    // 128-wide tiles take two k blocks per stage whenever three such stages
+    // fit: the producer's and the MMA issuer's barrier operations per stage
+    // cost more than a 128-wide k block's MMAs (about 256 cycles), and two
+    // blocks per stage halve them per block (P4 m128 sweep point: 24.7 ->
+    // 22.0 us).  256-wide tiles keep one block per stage and their deeper
+    // ring: their MMAs take about as long as the hand-offs, and with two
+    // blocks per stage only three stages fit (c4_quarter: 262 -> 269 us).
+    pl->atoms = bn == 128 && budget / (2 * (kASlotBytes + (int64_t)pl->b_slot_bytes)) >= 3 ? 2 : 1;
+    const int env_atoms = env_int("AGMM_ATOMS", 0);
+    if (env_atoms == 1 || env_atoms == 2) pl->atoms = env_atoms;
+    pl->key.atoms = pl->atoms;
+    const int64_t stage_bytes = (kASlotBytes + pl->b_slot_bytes) * pl->atoms;
     pl->stages = (int)std::min<int64_t>(kMaxStages, budget / stage_bytes);
     if (c.stages) pl->stages = std::min(pl->stages, c.stages);
     pl->splits = 1;

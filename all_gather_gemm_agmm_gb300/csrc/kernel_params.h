@@ -108,6 +108,14 @@ struct KernelKey {
                        // the X rows to the gathered LHS (agmm_run_gather)
 };
 
+// One instantiation of the fused kernel, chosen by select_*_kernel from a key
+// (nullptr: no such variant); each group of variants lives in its own
+// translation unit (agmm_select_*.cu).
+using KernelFn = void (*)(KernelParams);
+KernelFn select_swap_kernel(const KernelKey& k);
+KernelFn select_rows_kernel_a1(const KernelKey& k);
+KernelFn select_rows_kernel_a2(const KernelKey& k);
+
 // Largest dynamic shared memory a CTA may request (227 KiB on sm_100-class parts).
 constexpr size_t kMaxDynSmem = 232448;
 

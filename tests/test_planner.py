@@ -28,7 +28,8 @@ def preview(w, **kw):
 
 # (path, box_rows, whole_shards, chunks, tile_n, stages, row_groups, split bound);
 # row tiles in two-CTA clusters multiply as CTA pairs (half the Y tile per
-# CTA), hence 7 stages of 32 KiB; swapped tiles stage two k blocks at a time
+# CTA), hence 7 stages of 32 KiB at 256-wide tiles; 128-wide row tiles and
+# swapped tiles stage two k blocks at a time
 PINNED = {
     "c1_tiny": (1, 16, 1, 2, 32, 5, 2, 4),
     "c2_decode": (1, 64, 1, 4, 128, 3, 2, 9),
@@ -36,7 +37,8 @@ PINNED = {
     "c4_prefill": (0, 128, 0, 128, 256, 7, 1, 1),
     "sweep_P8_m8_nt": (1, 8, 1, 8, 64, 4, 1, 7),
     "sweep_P2_m1000_nt": (0, 128, 0, 16, 256, 7, 1, 1),
-    "sweep_P4_m128_rt": (0, 128, 1, 4, 128, 8, 1, 1),  # 128-wide: 256-wide gives 20 cluster tiles
+    # 128-wide (256-wide gives 20 cluster tiles), two k blocks per stage: 4 stages of 2 x 24 KiB
+    "sweep_P4_m128_rt": (0, 128, 1, 4, 128, 4, 1, 1),
 }
 
 
