@@ -124,8 +124,9 @@ typedef struct {
                        always a pair, so cluster_m 2 with cta_pair off is
                        AGMM_ERR_UNSUPPORTED)                                  */
   int stages;       /* pipeline stages, 2..8: an upper bound that shared
-                       memory may lower (a swapped k-split reduction that
-                       receives in shared memory may raise it)                */
+                       memory may lower (a swapped k-split reduction through
+                       distributed shared memory takes room for its receive
+                       buffer)                                                */
   int group_m;      /* row tiles: row-tile (pairs) per raster group, >= 1     */
   int stream_k;     /* row tiles: share a ragged last wave's k blocks         */
   int row_groups;   /* swapped tiles: groups of chunks (1, 2, 4, ...), each a
