@@ -244,3 +244,26 @@ def test_swap_reduction_routes(agmm, case):
         for s, os_ in same_split.items():
             for o in os_[1:]:
                 assert torch.equal(os_[0].view(torch.int16), o.view(torch.int16)), (case, s)
+
+
+@pytest.mark.parametrize("case", [(3, 200, 1024, 512, False), (4, 128, 1280, 512, True), (8, 130, 768, 1280, True)],
+                         ids=lambda c: "P{}_m{}_n{}".format(c[0], c[1], c[3]))
+def test_row_tiles_k_blocks_per_stage(agmm, case, monkeypatch):
+    # Row tiles stage one or two k blocks per pipeline step (the planner takes
+    # two for 128-wide tiles); both meet the oracle and, with the same tiles
+    # and k partition, agree bitwise (the MMAs accumulate in the same order).
+    P, m, k, n, rt = case
+    xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=23)
+    ref32, _ = oracle.agmm(xs_cpu, y_cpu, rt)
+    for bn in ("128", "256"):
+        if int(n) % int(bn):
+            continue
+        monkeypatch.setenv("AGMM_BN", bn)
+        outs = []
+        for atoms in ("1", "2"):
+            monkeypatch.setenv("AGMM_ATOMS", atoms)
+            o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=1)
+            assert plan.info()["path"] == 0 and plan.info()["tile_n"] == int(bn)
+            check(o, ref32, f"BN {bn} atoms {atoms} {plan.info()}")
+            outs.append(o)
+        assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), (case, bn)
