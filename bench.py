@@ -495,18 +495,25 @@ def bench_ours(args, w):
     unf_ms, gath_ms = uf["s_per_step"] * 1e3, gz["s_per_step"] * 1e3
     del wb.xcats
 
-    # end to end through the C ABI from pinned host memory.  Two steps are in
-    # flight: each slot has its own device buffers, plan, workspace and
-    # stream, so one step's uploads overlap the previous step's kernel and
-    # download.  Every step still uploads all of its inputs and reads its O.
+    # end to end through the C ABI from pinned host memory.  Three steps are
+    # in flight: each slot has its own device buffers, plan, workspace and
+    # stream, so one step's uploads overlap other steps' kernels and
+    # downloads.  Every step still uploads all of its inputs and reads its O.
+    # The same uploads and downloads without the kernel give the host link's
+    # own time per step, the bound of this number.
     e2e = None
     if not args.no_e2e:
         reps = wb.reps
         xs_h = [x.cpu().pin_memory() for x in reps[0][0]]
         y_h = reps[0][1].cpu().pin_memory()
+        n_slots = 3
         slots = []
-        for si in range(2):
-            xs_d, y_d, o_d = reps[si % len(reps)]
+        for si in range(n_slots):
+            if si < len(reps):
+                xs_d, y_d, o_d = reps[si]
+            else:
+                xs_d = [torch.empty_like(x) for x in reps[0][0]]
+                y_d, o_d = torch.empty_like(reps[0][1]), torch.empty_like(reps[0][2])
             pl = plan if si == 0 else agmm.Plan(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose,
                                                 f16=args.dtype == "f16")
             wsi = ws if si == 0 else pl.new_workspace()
@@ -517,31 +524,48 @@ def bench_ours(args, w):
 
         def e2e_steps(n):
             for i in range(n):
-                pl, wsi, st, xs_d, y_d, o_d, o_h = slots[i % 2]
+                pl, wsi, st, xs_d, y_d, o_d, o_h = slots[i % n_slots]
                 pl.run_host(xs_h, y_h, o_h, xs_d, y_d, o_d, w.my_id, wsi, st)
 
-        e2e_steps(4)
-        torch.cuda.synchronize()
-        barrier()
-        t0 = time.perf_counter()
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        ev0.record(slots[0][2])
-        slots[1][2].wait_event(ev0)
-        e2e_steps(Ke)
-        done = torch.cuda.Event()
-        done.record(slots[1][2])
-        slots[0][2].wait_event(done)
-        ev1.record(slots[0][2])
-        ev1.synchronize()
-        wall = time.perf_counter() - t0
+        def link_steps(n):
+            for i in range(n):
+                _, _, st, xs_d, y_d, o_d, o_h = slots[i % n_slots]
+                with torch.cuda.stream(st):
+                    for a, b in zip(xs_d, xs_h):
+                        a.copy_(b, non_blocking=True)
+                    y_d.copy_(y_h, non_blocking=True)
+                    o_h.copy_(o_d, non_blocking=True)
+
+        def timed_wall(fn, n):
+            fn(4)
+            torch.cuda.synchronize()
+            barrier()
+            t0 = time.perf_counter()
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev0.record(slots[0][2])
+            for sl in slots[1:]:
+                sl[2].wait_event(ev0)
+            fn(n)
+            for sl in slots[1:]:
+                done = torch.cuda.Event()
+                done.record(sl[2])
+                slots[0][2].wait_event(done)
+            ev1.record(slots[0][2])
+            ev1.synchronize()
+            wall = time.perf_counter() - t0
+            return max(ev0.elapsed_time(ev1) / 1000.0, wall)
+
+        e_el = timed_wall(e2e_steps, Ke)
         for pl, wsi, st, *_ in slots:
             pl.query_status(wsi, st)
-        e_el = max(ev0.elapsed_time(ev1) / 1000.0, wall)
+        link_el = timed_wall(link_steps, Ke)
         e_val, _ = aggregate_throughput(w.flops * Ke / 1e12, e_el, device)
         e2e = {"value": e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * (w.M * w.k + w.k * w.n),
                "d2h_bytes_per_step": 2 * w.M * w.n, "steps": Ke, "ms_per_step": e_el / Ke * 1e3,
-               "pipelining": "2 steps in flight (two device buffer sets, two streams)"}
+               "pipelining": f"{n_slots} steps in flight ({n_slots} device buffer sets, {n_slots} streams)",
+               "host_link_ms_per_step": link_el / Ke * 1e3,
+               "of_host_link_bound": link_el / e_el}
         del slots, xs_h, y_h
     R, per_rep, l2 = wb.R, w.unique_bytes, wb.l2
     del wb
