@@ -734,7 +734,7 @@ agmm_status_t launch_fused(agmm_plan_s* pl, const void* const* xs, const void* y
                            void* status, void* tail_ws, cudaStream_t stream, void* xcat = nullptr) {
   KernelParams& kpx = pl->params;
   // swapped tiles: the MMA thread stores the X boxes when asked; row tiles:
-  // the store warp of the store variant writes them to xcat
+  // the epilogue warps of the store variant copy the rows to xcat
   kpx.store_xcat = xcat != nullptr && pl->key.path == kPathSwap ? 1 : 0;
   kpx.xcat = xcat;
   kpx.ldx = pl->k;

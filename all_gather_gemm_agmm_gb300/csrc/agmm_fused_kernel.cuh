@@ -820,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         // it, so each (X rows, k block) is stored by the one n tile whose
         // share of the k range holds that k block: n tile t stores k blocks
         // [t*K/T, (t+1)*K/T) of its range, and the stores are spread evenly.
-        // (row tiles: the store warp does this)
+        // (row tiles: the store variant's epilogue warps copy it instead)
         bool store = false;
         int st_lo = 0, st_hi = 0;
         if constexpr (kPath == kPathRows) {

@@ -124,7 +124,7 @@ def test_gathered_lhs_argument_errors_and_pair_plans(agmm):
     with pytest.raises(agmm.AgmmError) as err:
         plan.run_gather(xs, y, o, xs[0], 0, ws)
     assert err.value.status == agmm.AGMM_ERR_INVALID_ARG
-    # a CTA-pair plan (the row-tile default): each CTA's store warp writes
+    # a CTA-pair plan (the row-tile default): each CTA's epilogue warps copy
     # its own rows
     pm, pk, pn = 256, 512, 256
     xs2, y2 = make_inputs(2, pm, pk, pn, False, seed=17)
@@ -158,8 +158,8 @@ ROW_SHAPES = [
 @pytest.mark.parametrize("cfg", ROW_FORMS, ids=str)
 @pytest.mark.parametrize("shape", ROW_SHAPES, ids=lambda c: "P{}_m{}_k{}_n{}".format(*c[:4]))
 def test_gathered_lhs_row_tile_forms(agmm, cfg, shape):
-    # Row tiles store the gathered LHS from a store warp in each CTA while the
-    # MMAs read the same stage; the gathered buffer is exact and O is bitwise
+    # Row tiles copy the gathered LHS from the shards with the epilogue warps
+    # while the main loop runs; the gathered buffer is exact and O is bitwise
     # the plain run's O under the same plan.
     P, m, k, n, rt = shape
     xs_cpu, y_cpu = make_inputs(P, m, k, n, rt, seed=18)
