@@ -62,7 +62,7 @@ class PlanInfo(ctypes.Structure):
         ("num_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("num_sms", ctypes.c_int),
         ("smem_bytes", ctypes.c_size_t), ("row_groups", ctypes.c_int), ("cluster_m", ctypes.c_int),
         ("cta_pair", ctypes.c_int), ("stream_k_tiles", ctypes.c_int), ("dsmem_reduce", ctypes.c_int),
-        ("config_source", ctypes.c_int),
+        ("config_source", ctypes.c_int), ("k_blocks_per_stage", ctypes.c_int),
     ]
 
 

@@ -1027,6 +1027,7 @@ agmm_status_t agmm_plan_info(agmm_plan_t plan, agmm_plan_info_t* info) {
   info->stream_k_tiles = plan->key.path == kPathSwap ? 0 : plan->sk_tiles;
   info->dsmem_reduce = plan->key.path == kPathSwap && plan->swap_dsmem ? 1 : 0;
   info->config_source = plan->config_source;
+  info->k_blocks_per_stage = plan->atoms;
   return AGMM_OK;
 }
 
@@ -1075,6 +1076,7 @@ agmm_status_t agmm_plan_preview(int P, int64_t m_per_device, int64_t k, int64_t 
   info->stream_k_tiles = pl.key.path == kPathSwap ? 0 : pl.sk_tiles;
   info->dsmem_reduce = pl.key.path == kPathSwap && pl.swap_dsmem ? 1 : 0;
   info->config_source = rc.source;
+  info->k_blocks_per_stage = pl.atoms;
   return AGMM_OK;
 }
 

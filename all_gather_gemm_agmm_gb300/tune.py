@@ -50,7 +50,7 @@ def _plan_key(info: Dict[str, int]) -> Tuple:
     """What makes two plans the same kernel launch."""
     return tuple(info[f] for f in ("path", "box_rows", "whole_shards", "tile_n", "stages", "splits", "num_ctas",
                                    "group_m", "row_groups", "cluster_m", "cta_pair", "stream_k_tiles",
-                                   "dsmem_reduce"))
+                                   "dsmem_reduce", "k_blocks_per_stage"))
 
 
 def candidates(P: int, m: int, k: int, n: int, rt: bool, f16: bool = False, num_sms: int = 152) -> List[Dict]:

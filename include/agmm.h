@@ -76,7 +76,7 @@ typedef struct {
   int chunks;        /* chunks in the whole ring-ordered row sequence            */
   int tile_m;        /* MMA M                                                    */
   int tile_n;        /* MMA N                                                    */
-  int tile_k;        /* k elements per pipeline stage                            */
+  int tile_k;        /* k elements per k block (one TMA box of X rows)           */
   int stages;        /* shared-memory pipeline depth                             */
   int splits;        /* k splits reduced inside a thread-block cluster           */
   int num_tiles;     /* output tiles                                             */
@@ -94,6 +94,8 @@ typedef struct {
   int config_source; /* 0: the planner's rules; 1: the tuned table (an entry
                         measured for this exact shape); 2: a caller's config or
                         AGMM_* environment overrides set at least one field     */
+  int k_blocks_per_stage; /* k blocks per pipeline stage: 1, or 2 where two fit
+                        three times (one barrier hand-off per two blocks)       */
 } agmm_plan_info_t;
 
 /*

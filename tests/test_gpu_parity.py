@@ -264,6 +264,7 @@ def test_row_tiles_k_blocks_per_stage(agmm, case, monkeypatch):
             monkeypatch.setenv("AGMM_ATOMS", atoms)
             o, plan = _run(agmm, xs_cpu, y_cpu, rt, my_id=1)
             assert plan.info()["path"] == 0 and plan.info()["tile_n"] == int(bn)
+            assert plan.info()["k_blocks_per_stage"] == int(atoms)
             check(o, ref32, f"BN {bn} atoms {atoms} {plan.info()}")
             outs.append(o)
         assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), (case, bn)

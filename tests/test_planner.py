@@ -26,19 +26,20 @@ def preview(w, **kw):
                              config={"tuned_table": False}, **kw)
 
 
-# (path, box_rows, whole_shards, chunks, tile_n, stages, row_groups, split bound);
+# (path, box_rows, whole_shards, chunks, tile_n, stages, row_groups, split bound,
+# k blocks per stage);
 # row tiles in two-CTA clusters multiply as CTA pairs (half the Y tile per
 # CTA), hence 7 stages of 32 KiB at 256-wide tiles; 128-wide row tiles and
 # swapped tiles stage two k blocks at a time
 PINNED = {
-    "c1_tiny": (1, 16, 1, 2, 32, 5, 2, 4),
-    "c2_decode": (1, 64, 1, 4, 128, 3, 2, 9),
-    "c3_mid": (0, 128, 0, 16, 256, 7, 1, 1),
-    "c4_prefill": (0, 128, 0, 128, 256, 7, 1, 1),
-    "sweep_P8_m8_nt": (1, 8, 1, 8, 64, 4, 1, 7),
-    "sweep_P2_m1000_nt": (0, 128, 0, 16, 256, 7, 1, 1),
+    "c1_tiny": (1, 16, 1, 2, 32, 5, 2, 4, 2),
+    "c2_decode": (1, 64, 1, 4, 128, 3, 2, 9, 2),
+    "c3_mid": (0, 128, 0, 16, 256, 7, 1, 1, 1),
+    "c4_prefill": (0, 128, 0, 128, 256, 7, 1, 1, 1),
+    "sweep_P8_m8_nt": (1, 8, 1, 8, 64, 4, 1, 7, 2),
+    "sweep_P2_m1000_nt": (0, 128, 0, 16, 256, 7, 1, 1, 1),
     # 128-wide (256-wide gives 20 cluster tiles), two k blocks per stage: 4 stages of 2 x 24 KiB
-    "sweep_P4_m128_rt": (0, 128, 1, 4, 128, 4, 1, 1),
+    "sweep_P4_m128_rt": (0, 128, 1, 4, 128, 4, 1, 1, 2),
 }
 
 
@@ -46,7 +47,7 @@ PINNED = {
 def test_pinned_workload_plans(name):
     info = preview(WORKLOADS[name])
     got = (info["path"], info["box_rows"], info["whole_shards"], info["chunks"], info["tile_n"], info["stages"],
-           info["row_groups"], info["splits"])
+           info["row_groups"], info["splits"], info["k_blocks_per_stage"])
     assert got == PINNED[name], (name, info)
 
 
