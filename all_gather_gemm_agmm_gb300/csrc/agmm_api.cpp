@@ -146,6 +146,7 @@ struct agmm_plan_s {
   int clock_khz = 2100000;  // peak SM clock of the planned device
   int group_chunks = 0;     // swap path: ring chunks per row group
   bool stream_k = true;     // rows path: share a ragged last wave's k blocks
+  bool stream_k_asked = false;  // rows path: the configuration set stream-K on (no fill rule)
   int config_source = 0;    // agmm_plan_info_t::config_source
   size_t tail_bytes = 0;  // workspace bytes for tail counters and partials
   // descriptor cache: tensor maps depend only on the X and Y pointers
@@ -505,6 +506,7 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
     pl->tmem_cols = 2 * bn;
     pl->group_m = c.group_m ? c.group_m : 8;
     pl->stream_k = c.stream_k != AGMM_CFG_OFF;
+    pl->stream_k_asked = c.stream_k == AGMM_CFG_ON;
   }
   pl->smem_bytes = tmem_safe_smem(1024 + (size_t)pl->stages * (kASlotBytes + pl->b_slot_bytes) * pl->atoms + kCtlBytes,
                                   pl->tmem_cols);
@@ -515,13 +517,17 @@ agmm_status_t choose_tiles(agmm_plan_s* pl, const agmm_tile_config_t& c, const a
 // co-resident.  Whole waves of cluster tiles are dealt round-robin; when the
 // tile count is not a multiple of the clusters, the last one to two waves' k
 // blocks are divided evenly over the clusters (stream-K), so no SM idles in a
-// ragged last wave.
+// ragged last wave -- unless that wave already fills two thirds of the
+// clusters: its idle clusters then cost less than stream-K's fix-up at the
+// end of the launch (an owner waits for its contributors' partials and sums
+// them), measured at about a third of a tile's time.  A configuration that
+// sets stream-K on keeps it whatever the fill.
 void size_rows_grid(agmm_plan_s* pl, int max_clusters) {
   const int cm = pl->key.cm;
   int G = std::max(1, std::min(pl->num_sms / cm, max_clusters));
   const int T = pl->num_tiles;
   int dp = T;
-  if (T % G != 0 && pl->stream_k) {
+  if (T % G != 0 && pl->stream_k && (pl->stream_k_asked || 3 * (T % G) < 2 * G)) {
     // Stream-K over the ragged last wave alone keeps its tiles together in
     // raster order (L2 reuse) as long as a tile is shared by at most about
     // three clusters; a thinner last wave also takes the wave before it.

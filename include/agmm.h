@@ -130,7 +130,9 @@ typedef struct {
                        distributed shared memory takes room for its receive
                        buffer)                                                */
   int group_m;      /* row tiles: row-tile (pairs) per raster group, >= 1     */
-  int stream_k;     /* row tiles: share a ragged last wave's k blocks         */
+  int stream_k;     /* row tiles: on = share a ragged last wave's k blocks
+                       (stream-K); auto = the same unless that wave fills at
+                       least two thirds of the clusters; off = whole tiles   */
   int row_groups;   /* swapped tiles: groups of chunks (1, 2, 4, ...), each a
                        separate MMA N; no group may be empty                  */
   int splits;       /* swapped tiles: k splits per cluster, 1..16: an upper
