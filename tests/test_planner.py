@@ -148,3 +148,25 @@ def test_resident_ctas_fit_tensor_memory(stages, monkeypatch):
         info = agmm.plan_preview(P, m, k, n, bool(rng.integers(0, 2)), num_sms=SMS)
         resident = 233472 // (info["smem_bytes"] + 1024)
         assert 1 <= resident and resident * _tmem_cols(info) <= 512, (P, m, k, n, info)
+
+
+def test_stream_k_fill_rule():
+    # A ragged last wave of cluster tiles goes to stream-K unless it already
+    # fills two thirds of the clusters (76 CTA pairs on 152 SMs); stream-K set
+    # on by the configuration applies whatever the fill.
+    tt = {"tuned_table": False}
+    cases = {"c4_quarter": (448, 0), "c4_prefill": (1792, 44), "c3_mid": (112, 36),
+             "sweep_P8_m4096_nt": (1280, 0), "sweep_P4_m1000_nt": (160, 84)}
+    for name, (tiles, sk) in cases.items():
+        w = WORKLOADS[name]
+        info = agmm.plan_preview(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, num_sms=SMS, config=tt)
+        assert (info["num_tiles"], info["stream_k_tiles"]) == (tiles, sk), name
+        ragged = tiles % (SMS // 2)
+        assert (sk == 0) == (ragged == 0 or 3 * ragged >= 2 * (SMS // 2)), name
+    w = WORKLOADS["c4_quarter"]
+    on = agmm.plan_preview(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, num_sms=SMS,
+                           config={"tuned_table": False, "stream_k": True})
+    assert on["stream_k_tiles"] == 448 % (SMS // 2)
+    off = agmm.plan_preview(w.P, w.m_per_device, w.k, w.n, w.rhs_transpose, num_sms=SMS,
+                            config={"tuned_table": False, "stream_k": False})
+    assert off["stream_k_tiles"] == 0
