@@ -202,8 +202,12 @@ struct Segment {
   int role;      // whole tile, owner of a split tile, or contributor
 };
 
-// The rows-path work of one cluster, in order: its data-parallel tiles, then
-// its contiguous share of the stream-K units (see KernelParams).
+// The rows-path work of one cluster, in order: its contiguous share of the
+// stream-K units (see KernelParams), then its data-parallel tiles.  Taking the
+// shared tiles first lets a stream-K owner's fix-up (waiting for its
+// contributors' partials, then summing them) run on the epilogue warps while
+// the main loop works through the whole tiles, instead of ending the launch;
+// every contributor's share is then done early in the launch as well.
 struct SegmentIter {
   int cid, nclusters, kblocks, dp_tiles, next_dp;
   int64_t u, hi;
@@ -221,13 +225,7 @@ struct SegmentIter {
   }
 
   __device__ __forceinline__ bool next(const KernelParams& p, int cm, int crank, Segment& s) {
-    if (next_dp < dp_tiles) {
-      s.tile = next_dp;
-      s.kb0 = 0;
-      s.kb1 = kblocks;
-      s.role = kSegWhole;
-      next_dp += nclusters;
-    } else if (u < hi) {
+    if (u < hi) {
       const int t = (int)(u / kblocks);
       s.tile = t;
       s.kb0 = (int)(u - (int64_t)t * kblocks);
@@ -235,6 +233,12 @@ struct SegmentIter {
       s.kb1 = (int)min((int64_t)kblocks, (int64_t)s.kb0 + left);
       s.role = (s.kb0 == 0) ? (s.kb1 == kblocks ? kSegWhole : kSegOwner) : kSegContrib;
       u += s.kb1 - s.kb0;
+    } else if (next_dp < dp_tiles) {
+      s.tile = next_dp;
+      s.kb0 = 0;
+      s.kb1 = kblocks;
+      s.role = kSegWhole;
+      next_dp += nclusters;
     } else {
       return false;
     }
