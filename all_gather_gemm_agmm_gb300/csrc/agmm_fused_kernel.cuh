@@ -202,12 +202,16 @@ struct Segment {
   int role;      // whole tile, owner of a split tile, or contributor
 };
 
-// The rows-path work of one cluster, in order: its contiguous share of the
-// stream-K units (see KernelParams), then its data-parallel tiles.  Taking the
-// shared tiles first lets a stream-K owner's fix-up (waiting for its
-// contributors' partials, then summing them) run on the epilogue warps while
-// the main loop works through the whole tiles, instead of ending the launch;
-// every contributor's share is then done early in the launch as well.
+// The rows-path work of one cluster: its contiguous share of the stream-K
+// units (see KernelParams) and its data-parallel tiles.  The plain kernel
+// takes the shared tiles first (kSkFirst): a stream-K owner's fix-up (waiting
+// for its contributors' partials, then summing them) then runs on the
+// epilogue warps while the main loop works through the whole tiles, instead
+// of ending the launch, and every contributor's share is done early.  The
+// variant that also copies the gathered LHS takes its whole tiles first: its
+// epilogue warps copy each segment's share of X before draining the segment,
+// and behind short stream-K segments that copy would hold up the
+// contributors' hand-offs.
 struct SegmentIter {
   int cid, nclusters, kblocks, dp_tiles, next_dp;
   int64_t u, hi;
@@ -224,8 +228,9 @@ struct SegmentIter {
     hi = base + units * (cluster_id + 1) / clusters;
   }
 
+  template <bool kSkFirst>
   __device__ __forceinline__ bool next(const KernelParams& p, int cm, int crank, Segment& s) {
-    if (u < hi) {
+    if (u < hi && (kSkFirst || next_dp >= dp_tiles)) {
       const int t = (int)(u / kblocks);
       s.tile = t;
       s.kb0 = (int)(u - (int64_t)t * kblocks);
@@ -634,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         uint32_t bytes;
         if constexpr (kPath == kPathRows) {
           Segment sg;
-          if (!iter.next(p, kCM, crank, sg)) break;
+          if (!iter.template next<!kStore>(p, kCM, crank, sg)) break;
           mt = sg.mt;
           nt = sg.nt;
           kb0 = sg.kb0;
@@ -829,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
         int st_lo = 0, st_hi = 0;
         if constexpr (kPath == kPathRows) {
           Segment sg;
-          if (!iter.next(p, kCM, crank, sg)) break;
+          if (!iter.template next<!kStore>(p, kCM, crank, sg)) break;
           kb0 = sg.kb0;
           kb1 = sg.kb1;
         } else {
@@ -965,7 +970,7 @@ __global__ void __launch_bounds__(kThreads, 1) agmm_fused_sm103a(const __grid_co
       uint32_t owner_parity = 0, publish_parity = 0;
       for (int tile = 0;; ++tile, ++it) {
         Segment sg;
-        if (!iter.next(p, kCM, crank, sg)) break;
+        if (!iter.template next<!kStore>(p, kCM, crank, sg)) break;
         if constexpr (kStore) {
           // while this segment's main loop runs: its share of the gathered LHS
           const int st_lo = (int)((int64_t)sg.nt * p.num_k_blocks / p.num_n_tiles);

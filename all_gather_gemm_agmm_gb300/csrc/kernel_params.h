@@ -62,7 +62,8 @@ struct __align__(128) KernelParams {
   // float32 partial in sk_partials[cluster][cluster rank] and count themselves
   // in sk_flags[tile - dp_tiles][cluster rank].  The owner waits for them,
   // adds the partials in k order and resets the counter to 0.  Each cluster
-  // works through its stream-K units first, then its whole tiles.
+  // works through its stream-K units first, then its whole tiles (the
+  // gathered-LHS variant: its whole tiles first).
   int dp_tiles;
   int sk_min_units;              // unused on the device; planner bookkeeping
   int* sk_flags;                 // [sk tiles][cluster rank] arrival counters (zero between runs)
