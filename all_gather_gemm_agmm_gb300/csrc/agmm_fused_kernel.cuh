@@ -437,35 +437,42 @@ __device__ __noinline__ void copy_x_rows(const KernelParams& p, const RingGeom& 
     src_row = ch.src_row;
     out_row = ch.out_row;
   }
+  // Warp w copies rows [32w, 32w + 32) of the tile; lane l first resolves row
+  // 32w + l (its chunk's shard, source and output rows), then the warp walks
+  // the rows kU at a time, each lane taking one 16-byte piece of each row, so
+  // that kU loads are in flight per thread without per-piece divisions.
+  const int r_mine = (t & ~31) + lane;
+  const int j_mine = r_mine >> p.box_shift;
+  const int rr_mine = r_mine & (p.box_rows - 1);
+  const int sh = __shfl_sync(0xffffffffu, shard, j_mine);
+  const int vl = __shfl_sync(0xffffffffu, valid, j_mine);
+  const int64_t sr = __shfl_sync(0xffffffffu, src_row, j_mine);
+  const int64_t orow = __shfl_sync(0xffffffffu, out_row, j_mine);
+  const bool ok_mine = rr_mine < vl;
+  const uint16_t* const src_mine =
+      static_cast<const uint16_t*>(p.xsrc[sh]) + (sr + rr_mine) * p.ldx + (int64_t)kb_a * kTileK;
+  uint16_t* const dst_mine = static_cast<uint16_t*>(p.xcat) + (orow + rr_mine) * p.ldx + (int64_t)kb_a * kTileK;
   const int ppr = (kb_b - kb_a) * (kTileK / 8);  // 16-byte pieces per row
-  const int64_t col0 = (int64_t)kb_a * kTileK;
-  const int units = kTileM * ppr;
-  uint16_t* const xcat = static_cast<uint16_t*>(p.xcat);
-  constexpr int U = 8;  // loads in flight per thread
-  for (int base = 0; base < units; base += 128 * U) {
-    uint4 v[U];
-    int64_t dst[U];
+  constexpr int kU = 16;                          // rows (loads) in flight per thread
+  for (int pc = lane; pc - lane < ppr; pc += 32) {
+#pragma unroll 1
+    for (int r0 = 0; r0 < 32; r0 += kU) {
+      uint4 v[kU];
+      uint16_t* dst[kU];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int idx = base + u * 128 + t;
-      const int r = min(idx / ppr, kTileM - 1);
-      const int pc = idx - r * ppr;
-      const int j = r >> p.box_shift;
-      const int rr = r & (p.box_rows - 1);
-      const int sh = __shfl_sync(0xffffffffu, shard, j);
-      const int vl = __shfl_sync(0xffffffffu, valid, j);
-      const int64_t sr = __shfl_sync(0xffffffffu, src_row, j);
-      const int64_t orow = __shfl_sync(0xffffffffu, out_row, j);
-      dst[u] = -1;
-      if (idx < units && rr < vl) {
-        const int64_t c = col0 + (int64_t)pc * 8;
-        v[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.xsrc[sh]) + (sr + rr) * p.ldx + c));
-        dst[u] = (orow + rr) * p.ldx + c;
+      for (int u = 0; u < kU; ++u) {
+        const uint16_t* s_ = reinterpret_cast<const uint16_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(src_mine), r0 + u));
+        uint16_t* d_ = reinterpret_cast<uint16_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst_mine), r0 + u));
+        const bool ok = __shfl_sync(0xffffffffu, ok_mine ? 1 : 0, r0 + u) != 0 && pc < ppr;
+        dst[u] = ok ? d_ + (int64_t)pc * 8 : nullptr;
+        if (ok) v[u] = __ldg(reinterpret_cast<const uint4*>(s_ + (int64_t)pc * 8));
       }
-    }
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (dst[u] >= 0) __stcs(reinterpret_cast<uint4*>(xcat + dst[u]), v[u]);  // streaming: not re-read
+      for (int u = 0; u < kU; ++u)
+        if (dst[u] != nullptr) __stcs(reinterpret_cast<uint4*>(dst[u]), v[u]);  // streaming: not re-read
+    }
   }
 }
 
