@@ -586,6 +586,7 @@ def bench_ours(args, w):
     if not args.no_sub:
         for name in [n for n in args.sub.split(",") if n and n != w.name]:
             subs[name] = sub_result(args, name, device, stream, peaks, peak_src)
+    sweep_smp = None if args.no_sub else sweep_sample(args, device, stream, peaks, peak_src)
 
     roof = roofline_of(w, s_step, peaks, peak_src,
                        sustained="sw_power_cap" in (clocks or {}).get("reasons", []))
@@ -608,6 +609,7 @@ def bench_ours(args, w):
         "with_gathered": {"ms_per_step": gath_ms, "steps": K, "batches": gz["batches"],
                           "vs_unfused": unf_ms / gath_ms, "cost_over_fused": gath_ms / ms_per_step},
         "sub_results": subs,
+        "sweep_sample": sweep_smp,
         "e2e": e2e,
         "gpu_launches": K,
         "gpu_launches_note": "fused kernel launches per timed batch (one per step)",
@@ -617,6 +619,40 @@ def bench_ours(args, w):
         result["cpu_baseline"] = cpu_oracle_sample(w, target_s=args.cpu_seconds, dtype=args.dtype)
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+SWEEP_SAMPLE = ("sweep_P2_m8_rt", "sweep_P8_m8_nt", "sweep_P4_m32_rt", "sweep_P2_m128_nt", "sweep_P8_m128_rt",
+                "sweep_P2_m1000_rt", "sweep_P4_m1000_nt", "sweep_P8_m4096_nt")
+
+
+def sweep_sample(args, device, stream, peaks, peak_src):
+    """Fused against gather-then-GEMM on a sample of the sweep spanning its P,
+    m and layouts, timed like the headline (K-step graphs over replicas larger
+    than L2, median of at least 7 batches) with shorter timed regions."""
+    import torch
+
+    from all_gather_gemm_agmm_gb300.inputs import WORKLOADS
+
+    points = []
+    for name in [n for n in args.sweep_sample.split(",") if n]:
+        w = WORKLOADS[name]
+        wb = WorkloadBench(w, device, args.dtype)
+        fused = wb.fused()
+        K = uniform_count(steps_for(estimate_step_s(fused, stream), args.steps or 20), device)
+        f, _ = measure(fused, K, args.warmup, stream, device, min_timed_s=0.15)
+        wb.plan.query_status(wb.ws, stream)
+        u, _ = measure(wb.unfused(), K, args.warmup, stream, device, min_timed_s=0.15)
+        wb.plan.query_status(wb.ws_unf, stream)
+        roof = roofline_of(w, f["s_per_step"], peaks, peak_src)
+        points.append({"point": name.replace("sweep_", ""), "fused_us": f["s_per_step"] * 1e6,
+                       "unfused_us": u["s_per_step"] * 1e6, "fused_speedup": u["s_per_step"] / f["s_per_step"],
+                       "bound": roof["bound"], "frac": roof["frac"], "steps": K, "batches": f["batches"]})
+        del wb, fused
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return {"points": points, "fused_faster_everywhere": all(q["fused_speedup"] > 1.0 for q in points),
+            "timing": "per point: K-step CUDA graphs over replicas > 3x L2, median of >= 7 batches, "
+                      "fused and unfused on the same replicas; max over ranks"}
 
 
 def bench_sweep(args):
@@ -729,6 +765,8 @@ def main(argv=None):
     ap.add_argument("--sub", default="c2_decode,c3_mid",
                     help="comma-separated workloads measured as sub-results of the same line")
     ap.add_argument("--sweep-points", default="", help="with --sweep: comma-separated sweep point names")
+    ap.add_argument("--sweep-sample", default=",".join(SWEEP_SAMPLE),
+                    help="sweep points timed fused against unfused in the default run ('' for none)")
     ap.add_argument("--profile-target", action="store_true",
                     help="only launch W + K steps of --path, eagerly, for a profiler (no timing)")
     ap.add_argument("--path", choices=["fused", "unfused", "gather"], default="fused")

@@ -57,3 +57,14 @@ def test_sweep_bounds_split_at_the_ridge():
         bound = bench.roofline_of(w, 1e-3, peaks, "measured")["bound"]
         assert bound == ("hbm" if w.flops / w.unique_bytes < ridge else "tensor")
         assert (bound == "hbm") == (w.M <= 256), name
+
+
+def test_sweep_sample_spans_the_sweep():
+    # the default benchmark line times fused against unfused on these points
+    pts = [WORKLOADS[n] for n in bench.SWEEP_SAMPLE]
+    assert {w.P for w in pts} == {2, 4, 8}
+    assert {w.m_per_device for w in pts} == {8, 32, 128, 1000, 4096}
+    assert {w.rhs_transpose for w in pts} == {False, True}
+    peaks, _ = bench.load_peaks()
+    bounds = {bench.roofline_of(w, 1e-3, peaks, "measured")["bound"] for w in pts}
+    assert bounds == {"hbm", "tensor"}
